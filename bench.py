@@ -1,0 +1,521 @@
+#!/usr/bin/env python3
+"""Throughput of the routed W4A16 MoE layer (moe_layer_forward) on GB300.
+
+One step = one pass of the whole layer over one batch of the workload:
+  decode (default): 48 distinct decode-shaped layers back to back, T=2 tokens
+      each (d_model 2048, d_ff 768, 128 experts, top-8, int4 g128 weights);
+      15.4 GB of distinct weights, so every layer reads its experts from HBM.
+  skew: one skewed prefill layer, P=4096 tokens, Zipf(1.1) expert load.
+  (prefill, large_decode, large_prefill, tiny are accepted too.)
+Metric: MoE-layer tokens/s = tokens routed through the layer per second
+(decode: 2 tokens x 48 layers per step).  The timed region replays a CUDA
+graph of the step on inputs already resident in HBM.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       [--impl ours|reference] [--no-secondary]
+Under torchrun (N > 1) every rank runs an independent replica (the layer has
+no cross-GPU exchange); value = all ranks' tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth as S  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (decode T=2, prefill P=4096); % HBM BW / % bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOADS = {
+    "decode": ("decode", 48),
+    "skew": ("skew", 1),
+    "prefill": ("prefill", 1),
+    "large_decode": ("large_decode", 1),
+    "large_prefill": ("large_prefill", 1),
+    "tiny": ("tiny", 1),
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# --------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def file_sha(path):
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh).get(kernel_key)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src) or file_sha(src) != d["source_sha"]:
+        return None  # kernel changed since the counters were taken
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    Q = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 10:
+                continue
+            if self.uuid and f[1] != self.uuid:
+                continue
+            rows.append(f)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][3]) if rows[0][3].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[4]) for r in rows if r[4].replace(".", "").isdigit()), default=None)}
+
+
+# --------------------------------------------------------------------------
+class Workload:
+    """Synthetic layers of one configuration, resident on the device."""
+
+    def __init__(self, M, torch, name, device):
+        self.cfg_name, self.L = WORKLOADS[name]
+        self.name = name
+        cfg = S.CONFIGS[self.cfg_name]
+        self.cfg = cfg
+        t0 = time.time()
+        self.host_w = [S.layer_weights(cfg, l) for l in range(self.L)]
+        self.host_x = [S.activations(cfg, l) for l in range(self.L)]
+        self.host_lg = [S.router_logits(cfg, l) for l in range(self.L)]
+        log(f"[bench] generated {self.L} layer(s) of {cfg.name} in {time.time() - t0:.1f}s")
+        self.layers = [M.Layer.from_numpy(w, device) for w in self.host_w]
+        self.x = [torch.from_numpy(x.view(np.int16)).to(device).view(torch.bfloat16) for x in self.host_x]
+        self.lg = [torch.from_numpy(g).to(device) for g in self.host_lg]
+        self.out = [torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=device) for _ in range(self.L)]
+        self.ids = [torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=device) for _ in range(self.L)]
+        self.calls = [M.LayerCall(layer, cfg.T, cfg.k, device=device) for layer in self.layers]
+        self.weight_bytes = sum(layer.nbytes() for layer in self.layers)
+
+    def step(self, stream):
+        for l in range(self.L):
+            self.calls[l](self.x[l], self.lg[l], self.out[l], self.ids[l], stream=stream)
+
+    def tokens_per_step(self):
+        return self.cfg.T * self.L
+
+
+def expert_bytes(cfg, which):
+    """Algorithmic bytes of one expert's gate_up or down matrix (codes + fp16 scale + zero)."""
+    n = (2 * cfg.f * cfg.d) if which == "gate_up" else (cfg.d * cfg.f)
+    return n // 2 + 4 * (n // 128)
+
+
+def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=True):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    cfg = wl.cfg
+    with torch.cuda.stream(s):
+        # eager warm-up (also configures kernels and checks the error word)
+        for _ in range(max(1, warmup)):
+            wl.step(s)
+        s.synchronize()
+        for c in wl.calls:
+            e = M.get_device_error(c.ws, s)
+            if e != 0:
+                raise RuntimeError(f"device error {M.status_str(e)}")
+        # eager timing (host launch cost included)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            wl.step(s)
+        e1.record(s)
+        s.synchronize()
+        eager_ms = e0.elapsed_time(e1) / steps
+        # one CUDA graph per step
+        n0 = M.kernel_launches()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            wl.step(s)
+        launches_per_step = M.kernel_launches() - n0
+        for _ in range(warmup):
+            g.replay()
+        s.synchronize()
+
+    # ---------------------------------------------------------- timed region
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        pass
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(uuid)
+    with sampler:
+        time.sleep(0.3)
+        with torch.cuda.stream(s):
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(s)
+            for _ in range(steps):
+                g.replay()
+            t1.record(s)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    ms = t0.elapsed_time(t1) / steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = wl.tokens_per_step() * world
+    value = tokens / (ms / 1e3)
+
+    # -------------------------------------- stage events of the same step (graph)
+    prof = M.StageProfiler(wl.L)
+    with torch.cuda.stream(s):
+        with prof:
+            gp = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp, stream=s):
+                wl.step(s)
+        stage_sum = np.zeros(5)
+        per_layer = np.zeros((wl.L, 5))
+        reps = max(3, min(steps, 10))
+        for _ in range(reps):
+            gp.replay()
+            st = np.array(prof.stage_ms())
+            per_layer += st
+            stage_sum += st.sum(0)
+        per_layer /= reps
+        stage_sum /= reps
+    uniq = [len(np.unique(i.cpu().numpy())) for i in wl.ids]
+    counts_R = cfg.T * cfg.k
+
+    decode_regime = counts_R <= 64
+    if decode_regime:
+        # dominant kernel: gate_up GEMV; bytes = touched experts' gate+up rows
+        gu_bytes = np.array([u * expert_bytes(cfg, "gate_up") + cfg.T * cfg.d * 2 for u in uniq], dtype=np.float64)
+        dn_bytes = np.array([u * expert_bytes(cfg, "down") for u in uniq], dtype=np.float64)
+        t_gu = per_layer[:, 2] / 1e3
+        t_dn = per_layer[:, 3] / 1e3
+        achieved = float(gu_bytes.sum() / t_gu.sum() / 1e9)
+        peak = float(peaks["hbm_gbs"])
+        pair = float((gu_bytes.sum() + dn_bytes.sum()) / (t_gu.sum() + t_dn.sum()) / 1e9)
+        tr = traffic_for("gemv_gateup_decode")
+        roofline = {"bound": "hbm", "kernel": "gemv_w4_kernel<gate_up>", "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": (round(tr["dram_bytes_per_launch"]) if tr else None),
+                    "algorithmic_bytes_per_launch": round(float(gu_bytes.mean())),
+                    "avg_launch_us": round(float(t_gu.mean() * 1e6), 2),
+                    "peak_source": peak_src,
+                    "expert_gemms_pair": {"achieved": round(pair, 1), "frac": round(pair / peak, 4),
+                                          "down_avg_us": round(float(t_dn.mean() * 1e6), 2)}}
+    else:
+        R = counts_R
+        fl_gu = 2.0 * R * 2 * cfg.f * cfg.d
+        fl_dn = 2.0 * R * cfg.f * cfg.d
+        t_gu = per_layer[:, 2].mean() / 1e3
+        t_dn = per_layer[:, 3].mean() / 1e3
+        achieved = fl_gu / t_gu / 1e12
+        peak = float(peaks["bf16_tflops"])
+        both = (fl_gu + fl_dn) / (t_gu + t_dn) / 1e12
+        tr = traffic_for("tc_gateup_" + wl.name)
+        roofline = {"bound": "tensor", "kernel": "tc_grouped_kernel<gate_up>", "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "traffic": (round(tr["dram_bytes_per_launch"]) if tr else None),
+                    "flops_per_launch": fl_gu, "avg_launch_us": round(t_gu * 1e6, 2), "peak_source": peak_src,
+                    "expert_gemms_pair": {"achieved": round(both, 1), "frac": round(both / peak, 4),
+                                          "down_avg_us": round(t_dn * 1e6, 2)},
+                    "weight_bytes_touched": float(sum(uniq) / len(uniq) * (expert_bytes(cfg, "gate_up") +
+                                                                          expert_bytes(cfg, "down")))}
+    stages = {k: round(float(v) * 1e3 / wl.L, 2) for k, v in
+              zip(["route", "permute", "gate_up", "down", "combine"], stage_sum)}
+
+    # ------------------------------------------------------------------ e2e
+    e2e = None
+    if want_e2e:
+        hx = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in wl.host_x]
+        hl = [torch.from_numpy(gl).pin_memory() for gl in wl.host_lg]
+        ho = [torch.empty((cfg.T, cfg.d), dtype=torch.int16).pin_memory() for _ in range(wl.L)]
+        h2d = sum(a.numel() * a.element_size() for a in hx) + sum(a.numel() * a.element_size() for a in hl)
+        d2h = sum(a.numel() * a.element_size() for a in ho)
+        with torch.cuda.stream(s):
+            def e2e_step():
+                for l in range(wl.L):
+                    wl.x[l].view(torch.int16).copy_(hx[l], non_blocking=True)
+                    wl.lg[l].copy_(hl[l], non_blocking=True)
+                g.replay()
+                for l in range(wl.L):
+                    ho[l].copy_(wl.out[l].view(torch.int16), non_blocking=True)
+            for _ in range(warmup):
+                e2e_step()
+            s.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(s)
+            for _ in range(steps):
+                e2e_step()
+            a1.record(s)
+            s.synchronize()
+        ems = a0.elapsed_time(a1) / steps
+        if world > 1:
+            tt = torch.tensor([ems], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            ems = float(tt.item())
+        e2e = {"value": round(tokens / (ems / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ems, 4),
+               "path": "pinned host x/logits -> device, graph replay of moe_layer_forward x L, out -> pinned host"}
+
+    return {
+        "value": value, "ms_per_step": ms, "eager_ms_per_step": eager_ms, "roofline": roofline,
+        "stages_us_per_layer": stages, "gpu_launches": int(launches_per_step * steps),
+        "launches_per_step": int(launches_per_step), "clocks": sampler.summary(), "e2e": e2e,
+        "uniq_experts_mean": float(np.mean(uniq)),
+    }
+
+
+# --------------------------------------------------------------------------
+def cpu_baseline(wl_name, budget_s=15.0, max_units=None):
+    """The oracle, as it stands, on the host cores: a bounded sample of the workload."""
+    import oracle as O
+    cfg_name, L = WORKLOADS[wl_name]
+    cfg = S.CONFIGS[cfg_name]
+    t_used = 0.0
+    tokens = 0
+    layers_done = 0
+    sample_desc = ""
+    t_start = time.time()
+    for l in range(L if cfg.T <= 64 else 1):
+        W = S.layer_weights(cfg, l)
+        x = S.activations(cfg, l)
+        lg = S.router_logits(cfg, l)
+
+        def ge(e, W=W):
+            return {k: v[e] for k, v in W.items()}
+        if cfg.T <= 64:
+            t0 = time.perf_counter()
+            O.layer_forward(x, lg, ge, cfg.E, cfg.d, cfg.f, cfg.k)
+            t_used += time.perf_counter() - t0
+            tokens += cfg.T
+            layers_done += 1
+            sample_desc = f"{layers_done} of {L} {cfg.name} layers (T={cfg.T} each), whole layer"
+        else:
+            # large batch: a bounded sample of tokens through the same layer
+            rng = np.random.default_rng(0)
+            n = 16
+            toks = np.sort(rng.choice(cfg.T, size=n, replace=False))
+            t0 = time.perf_counter()
+            O.layer_forward_tokens(x, lg, ge, cfg.E, cfg.d, cfg.f, cfg.k, toks)
+            t_used += time.perf_counter() - t0
+            tokens += n
+            sample_desc = f"{n} of {cfg.T} tokens of one {cfg.name} layer (all their experts)"
+        if t_used >= budget_s or time.time() - t_start > 3 * budget_s:
+            break
+        if max_units and layers_done >= max_units:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(tokens / t_used, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample_desc, "seconds": round(t_used, 2)}
+
+
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, world, local = dist_env()
+    cfg_name, L = WORKLOADS[args.workload]
+    cfg = S.CONFIGS[cfg_name]
+    config = {"workload": f"{args.workload}: {cfg.name} layer x{L}, T={cfg.T}, d_model={cfg.d}, d_ff={cfg.f}, "
+                          f"E={cfg.E}, top-{cfg.k}, int4 g128 (fp16 scale+zero)",
+              "T": cfg.T, "layers": L, "d_model": cfg.d, "d_ff": cfg.f, "E": cfg.E, "k": cfg.k,
+              "l2": "inputs larger than L2",
+              "parallelism": f"replicas x{world}"}
+
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle, as it stands, on the host cores.
+        # Each step is a bounded sample of the same workload: one decode layer
+        # (T tokens) per step, or a 16-token sample of a prefill layer.
+        if rank != 0:
+            return 0
+        import oracle as O
+        t_wall = time.time()
+        big = cfg.T > 64
+        rng = np.random.default_rng(0)
+
+        def one_step(i):
+            l = i % L
+            W = S.layer_weights(cfg, l)
+            x = S.activations(cfg, l)
+            lg = S.router_logits(cfg, l)
+
+            def ge(e, W=W):
+                return {k: v[e] for k, v in W.items()}
+            t0 = time.perf_counter()
+            if big:
+                toks = np.sort(rng.choice(cfg.T, size=16, replace=False))
+                O.layer_forward_tokens(x, lg, ge, cfg.E, cfg.d, cfg.f, cfg.k, toks)
+                n = 16
+            else:
+                O.layer_forward(x, lg, ge, cfg.E, cfg.d, cfg.f, cfg.k)
+                n = cfg.T
+            return time.perf_counter() - t0, n
+
+        for i in range(args.warmup):
+            one_step(i)
+        times, toks = [], 0
+        for i in range(args.steps):
+            dt, n = one_step(args.warmup + i)
+            times.append(dt)
+            toks += n
+        value = toks / sum(times)
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        sample = (f"per step: 16 of {cfg.T} tokens of one {cfg.name} layer" if big else
+                  f"per step: one of {L} {cfg.name} layers (T={cfg.T}), whole layer")
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "wall_s": round(time.time() - t_wall, 1)}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from bit_quantized_expert_moe_gb300 import build as B
+    if rank == 0:
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+    import bit_quantized_expert_moe_gb300 as M
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda", local)
+
+    wl = Workload(M, torch, args.workload, dev)
+    config["l2"] = (f"inputs larger than L2 ({wl.weight_bytes / 1e9:.1f} GB of distinct expert weights "
+                    f"across the step; no flush needed)")
+    res = measure(M, torch, wl, args.steps, args.warmup, rank, world, peaks, peak_src)
+    del wl
+    torch.cuda.empty_cache()
+
+    secondary = None
+    if not args.no_secondary and args.workload == "decode":
+        wl2 = Workload(M, torch, "skew", dev)
+        steps2 = max(5, args.steps)
+        r2 = measure(M, torch, wl2, steps2, args.warmup, rank, world, peaks, peak_src, want_e2e=True)
+        secondary = {"workload": "skew: one prefill layer, P=4096, Zipf(1.1) load, d_model=2048, d_ff=768, E=128, top-8",
+                     "value": round(r2["value"], 1), "unit": "tokens/s", "ms_per_step": round(r2["ms_per_step"], 4),
+                     "eager_ms_per_step": round(r2["eager_ms_per_step"], 4), "roofline": r2["roofline"],
+                     "stages_us_per_layer": r2["stages_us_per_layer"], "gpu_launches": r2["gpu_launches"],
+                     "clocks": r2["clocks"], "e2e": r2["e2e"]}
+        del wl2
+        torch.cuda.empty_cache()
+
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(args.workload, budget_s=12.0)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(res["value"], 1), "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded int4 codes, fp16 scales, bf16 N(0,1) activations, fp32 logits)",
+                "config": config, "roofline": res["roofline"], "cpu_baseline": base, "e2e": res["e2e"],
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
+                "eager_ms_per_step": round(res["eager_ms_per_step"], 4),
+                "stages_us_per_layer": res["stages_us_per_layer"], "uniq_experts_mean": res["uniq_experts_mean"],
+                "timing": "CUDA graph of the step replayed K times between two events on its stream; "
+                          "barrier + synchronize on both sides; max over ranks",
+                "prefill": secondary}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

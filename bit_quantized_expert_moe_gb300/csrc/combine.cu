@@ -1,0 +1,59 @@
+// Stage 4: router-weighted combine back to token order.
+//
+// out[t][n] = sum_{j<k} w[t][j] * y_perm[inv[t*k+j]][n], fp32 accumulation in
+// slot order j = 0..k-1, one rounding to bf16 at the end.  Each thread owns
+// 8 consecutive features of one token (16-byte loads and stores); the grid is
+// a multiple of the SM count and strides over (token, 8-feature chunk).
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y_perm,
+                                                      const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ w, int T, int k, int d,
+                                                      uint16_t* __restrict__ out) {
+    const int chunks = d / 8;
+    const long long total = (long long)T * chunks;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(idx / chunks);
+        const int c = (int)(idx % chunks);
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int pos = inv[(size_t)t * k + j];
+            if ((unsigned)pos >= (unsigned)(T * k)) continue;  // not a permutation entry
+            const float wj = w[(size_t)t * k + j];
+            const uint4 v = *reinterpret_cast<const uint4*>(y_perm + (size_t)pos * d + c * 8);
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(wj, __uint_as_float(u[i] << 16), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj, __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
+            }
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(out + (size_t)t * d + c * 8) = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv, const float* w, int T, int k,
+                           int d, uint16_t* out, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const long long work = (long long)T * (d / 8);
+    const int per_wave = num_sms() * 8;  // 8 CTAs of 256 threads per SM
+    const int blocks = (int)std::min<long long>(per_wave, (work + 255) / 256);
+    combine_kernel<<<blocks, 256, 0, s>>>(y_perm, inv, w, T, k, d, out);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace moe

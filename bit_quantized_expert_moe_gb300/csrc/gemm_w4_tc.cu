@@ -1,0 +1,473 @@
+// Stage 3, prefill regime: grouped W4A16 GEMM on the 5th-generation tensor
+// cores (tcgen05, TMEM accumulators, TMA).
+//
+// "Performance and verification", section "Why it is fast": the routed
+// experts of a prompt run as grouped tensor-core GEMMs; "Measured results",
+// section Speed: the prefill path dequantises the 4-bit weights to 16-bit and
+// runs a dense GEMM.  Here the dequantisation happens tile by tile in shared
+// memory, never in HBM.
+//
+// Shapes (swap-AB: weight rows are the MMA's M, tokens its N):
+//   D[m][n] = sum_k A[m][k] * B[n][k]     M = 128 weight rows, N <= 256 tokens
+//   A = dequantised weights (bf16, written by the dequant warps, SW128 K-major)
+//   B = activation rows of one expert segment (bf16, TMA, SW128 K-major)
+// A work item is (token tile of one expert, block of 128 weight rows); a
+// persistent CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...
+//
+// gate_up: the 128 A rows of a block hold 64 gate rows and the 64 matching up
+// rows, interleaved by 16 inside each 32-lane TMEM quarter, so one thread's
+// lane and the lane 16 above it carry gate and up of the same feature; the
+// epilogue pairs them with one shuffle and writes h = SiLU(g) * u (bf16).
+// down: 128 consecutive rows of W2; the epilogue writes y rows (bf16).
+//
+// Warp roles (512 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
+// 2-3 idle, 4-11 dequantisation, 12-15 epilogue (TMEM lane quarters 0..3).
+// Every wait is bounded in time; a timeout sets the error word, every role
+// leaves its loop, in-flight copies and MMAs are drained, TMEM is freed.
+#include <cstdio>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;                  // A rows per item
+constexpr int BK = 64;                   // K per stage: one 128-byte swizzle row of bf16
+constexpr int BN = TILE_ROWS;            // max tokens per item (256)
+constexpr int A_BYTES = BM * BK * 2;     // 16 KB
+constexpr int B_BYTES = BN * BK * 2;     // 32 KB
+constexpr int P_BYTES = BM * BK / 2;     // 4 KB of packed codes
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + P_BYTES;
+constexpr int B_BOX_ROWS = 32;           // activation rows per TMA box
+constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
+constexpr int THREADS = 512;
+constexpr int DQ_WARP0 = 4, DQ_WARPS = 8;
+constexpr int EP_WARP0 = 12;
+constexpr uint32_t TMEM_COLS = 512;      // two accumulators of 256 fp32 columns
+
+struct TcParams {
+    int E, d, f, R;
+    int K;        // reduction length (d for gate_up, f for down)
+    int NFB;      // weight-row blocks per expert
+    const uint16_t* wsc;   // scales [E * rows_per_expert][K/128]
+    const uint16_t* wz;    // zeros
+    const Tile* tiles;
+    const DevPlan* plan;
+    uint16_t* out;         // h [R][f] or y [R][d]
+    int out_ld;            // f or d
+    const float* row_w;
+    uint32_t* err;
+};
+
+__host__ __device__ constexpr size_t scale_bytes(int K) { return (size_t)2 * 2 * BM * (K / 128) * 2; }
+__host__ __device__ constexpr size_t tc_smem_bytes(int S, int K) {
+    return (size_t)S * STAGE_BYTES + scale_bytes(K) + 256 + 1024;
+}
+
+template <bool GATEUP>
+__device__ __forceinline__ void item_rows(const TcParams& p, int item, int& e, int& row0, int& nrows,
+                                          int& fb) {
+    const int ti = item / p.NFB;
+    fb = item - ti * p.NFB;
+    const Tile t = p.tiles[ti];
+    e = t.expert;
+    row0 = t.row0;
+    nrows = t.nrows;
+}
+
+// Global weight row of A row r of block fb of expert e.
+template <bool GATEUP>
+__device__ __forceinline__ size_t a_global_row(const TcParams& p, int e, int fb, int r) {
+    if (GATEUP) {
+        const int q = r >> 5, i = r & 31;
+        const size_t base = (size_t)e * 2 * p.f + (size_t)fb * 64 + 16 * q;
+        return (i < 16) ? base + i : base + p.f + (i - 16);
+    } else {
+        return (size_t)e * p.d + (size_t)fb * BM + r;
+    }
+}
+
+// Row of the packed-code stage buffer that holds A row r.
+template <bool GATEUP>
+__device__ __forceinline__ int a_packed_row(int r) {
+    if (GATEUP) {
+        const int q = r >> 5, i = r & 31;
+        return (i < 16) ? 16 * q + i : 64 + 16 * q + (i - 16);
+    } else {
+        return r;
+    }
+}
+
+// Wait that ignores the abort flag (used to drain in-flight work at teardown).
+__device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
+    if (tc::mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > tc::WAIT_LIMIT_NS) { set_error(err, ERRBIT_TIMEOUT); return; }
+    }
+}
+
+template <bool GATEUP, int S>
+__global__ void __launch_bounds__(THREADS, 1)
+tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+                  TcParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* gbase = smem_raw + (base - raw);
+
+    const uint32_t sA = base;
+    const uint32_t sB = base + S * A_BYTES;
+    const uint32_t sP = base + S * (A_BYTES + B_BYTES);
+    const int G = p.K / 128;
+    uint16_t* sScale = reinterpret_cast<uint16_t*>(gbase + S * STAGE_BYTES);  // [2][BM][G]
+    uint16_t* sZero = sScale + 2 * BM * G;                                     // [2][BM][G]
+    const uint32_t bars = base + S * STAGE_BYTES + (uint32_t)scale_bytes(p.K);
+    // barrier layout: full[S], afull[S], empty[S], accfull[2], accempty[2], done
+    const uint32_t bar_full = bars, bar_afull = bars + 8 * S, bar_empty = bars + 16 * S;
+    const uint32_t bar_accfull = bars + 24 * S, bar_accempty = bar_accfull + 16, bar_done = bar_accempty + 16;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + S * STAGE_BYTES + scale_bytes(p.K) + 8 * (3 * S + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_items = p.plan->n_tiles * p.NFB;
+    const int NK = p.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            tc::mbar_init(bar_full + 8 * s, 1);
+            tc::mbar_init(bar_afull + 8 * s, DQ_WARPS);
+            tc::mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(bar_accfull + 8 * b, 1);
+            tc::mbar_init(bar_accempty + 8 * b, 4);
+        }
+        tc::mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32((const void*)tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&map_w);
+            tc::tma_prefetch_desc(&map_x);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;  // per stage: last issued phase parity
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                int e, row0, nrows, fb;
+                item_rows<GATEUP>(p, item, e, row0, nrows, fb);
+                const int nbox = ceil_div(nrows, B_BOX_ROWS);
+                const int wrow_a = GATEUP ? e * 2 * p.f + fb * 64 : e * p.d + fb * BM;
+                const int wrow_b = GATEUP ? wrow_a + p.f : wrow_a + 64;
+                for (int kc = 0; kc < NK; ++kc) {
+                    if (!tc::mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    const uint32_t fbar = bar_full + 8 * stage;
+                    tc::mbar_arrive_expect_tx(fbar, P_BYTES + nbox * B_BOX_BYTES);
+                    const uint32_t dp = sP + stage * P_BYTES;
+                    tc::tma_load_2d(dp, &map_w, fbar, kc * (BK / 8), wrow_a);
+                    tc::tma_load_2d(dp + P_BYTES / 2, &map_w, fbar, kc * (BK / 8), wrow_b);
+                    const uint32_t db = sB + stage * B_BYTES;
+                    for (int b = 0; b < nbox; ++b)
+                        tc::tma_load_2d(db + b * B_BOX_BYTES, &map_x, fbar, kc * BK, row0 + b * B_BOX_ROWS);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            // drain: every issued stage's copies must have landed before exit
+            for (int s = 0; s < S; ++s)
+                if (issued_mask >> s & 1u) mbar_drain_wait(bar_full + 8 * s, (issued_phase >> s) & 1u, p.err);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int ic = 0;
+            bool ok = true, any = false;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+                int e, row0, nrows, fb;
+                item_rows<GATEUP>(p, item, e, row0, nrows, fb);
+                const int N = ceil_div(nrows, 16) * 16;
+                const uint32_t idesc = tc::idesc_bf16_f32(BM, N);
+                const int buf = ic & 1;
+                const uint32_t aph = (ic >> 1) & 1;
+                if (!tc::mbar_wait(bar_accempty + 8 * buf, aph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * 256;
+                for (int kc = 0; kc < NK; ++kc) {
+                    if (!tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err) ||
+                        !tc::mbar_wait(bar_afull + 8 * stage, phase, abort_flag, p.err)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t a0 = sA + stage * A_BYTES, b0 = sB + stage * B_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        tc::mma_bf16(d_tmem, tc::sw128_kmajor_desc(a0 + ks * 32), tc::sw128_kmajor_desc(b0 + ks * 32),
+                                     idesc, (kc | ks) != 0);
+                    }
+                    tc::mma_commit(bar_empty + 8 * stage);
+                    any = true;
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit(bar_accfull + 8 * buf);
+            }
+            // drain: all issued MMAs complete before TMEM is released
+            if (any) {
+                tc::mma_commit(bar_done);
+                mbar_drain_wait(bar_done, 0, p.err);
+            }
+        }
+    } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + DQ_WARPS) {
+        // ------------------------------------------------------ dequantisers
+        // Warp dw owns A rows dw*16 .. dw*16+15 of every stage; it prefetches
+        // those rows' scales and zeros itself (4-byte cp.async), so only warp-
+        // level synchronisation is needed.  Waits are made warp-uniform.
+        const int dt = threadIdx.x - DQ_WARP0 * 32;
+        const int dw = dt >> 5;
+        const int w = lane & 7;
+        auto prefetch_scales = [&](int item, int buf) {
+            int e, row0, nrows, fb;
+            item_rows<GATEUP>(p, item, e, row0, nrows, fb);
+            const int pairs = G / 2;
+            for (int idx = lane; idx < 16 * pairs; idx += 32) {
+                const int r = dw * 16 + idx / pairs, gp = idx % pairs;
+                const size_t grow = a_global_row<GATEUP>(p, e, fb, r);
+                const size_t src = grow * G + 2 * gp;
+                const size_t dst = ((size_t)buf * BM + r) * G + 2 * gp;
+                cp_async4(smem_u32(sScale + dst), p.wsc + src);
+                cp_async4(smem_u32(sZero + dst), p.wz + src);
+            }
+        };
+        int stage = 0;
+        uint32_t phase = 0;
+        int ic = 0;
+        bool ok = true;
+        if ((int)blockIdx.x < n_items) prefetch_scales(blockIdx.x, 0);
+        cp_async_commit();
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+            const int sbuf = ic & 1;
+            __syncwarp();  // the warp is done with the buffer the next prefetch overwrites
+            if (item + (int)gridDim.x < n_items) prefetch_scales(item + gridDim.x, sbuf ^ 1);
+            cp_async_commit();
+            cp_async_wait<1>();
+            __syncwarp();  // this item's scales visible to the whole warp
+            int r_it[4], prow[4];
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                r_it[it] = dw * 16 + it * 4 + (lane >> 3);
+                prow[it] = a_packed_row<GATEUP>(r_it[it]);
+            }
+            float2 sc[4], cc[4];  // per row: (s*2^11, s*2^7), (-(2^11+z)s, -(2^7+z)s)
+            for (int kc = 0; kc < NK; ++kc) {
+                ok = tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                if ((kc & 1) == 0) {
+                    const int g = kc >> 1;
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const size_t si = ((size_t)sbuf * BM + r_it[it]) * G + g;
+                        const float s = half_bits_to_float(sScale[si]);
+                        const float z = half_bits_to_float(sZero[si]);
+                        sc[it] = make_float2(s * 2048.f, s * 128.f);
+                        cc[it] = make_float2(-(2048.f + z) * s, -(128.f + z) * s);
+                    }
+                }
+                const uint32_t* pk = reinterpret_cast<const uint32_t*>(gbase + (sP - base) + stage * P_BYTES);
+                const uint32_t a0 = sA + stage * A_BYTES;
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const uint32_t word = pk[prow[it] * 8 + w];
+                    float2 v[4];
+                    nib8_magic(word, v);
+                    // v[m] = (odd code, even code) for pairs (3,4), (1,2), (5,6), (7,0)
+                    const float2 q34 = ffma2(v[0], sc[it], cc[it]);
+                    const float2 q12 = ffma2(v[1], sc[it], cc[it]);
+                    const float2 q56 = ffma2(v[2], sc[it], cc[it]);
+                    const float2 q70 = ffma2(v[3], sc[it], cc[it]);
+                    const uint32_t o0 = pack_bf16x2(q70.y, q12.x);  // k0, k1
+                    const uint32_t o1 = pack_bf16x2(q12.y, q34.x);  // k2, k3
+                    const uint32_t o2 = pack_bf16x2(q34.y, q56.x);  // k4, k5
+                    const uint32_t o3 = pack_bf16x2(q56.y, q70.x);  // k6, k7
+                    const int r = r_it[it];
+                    const uint32_t dst = a0 + (r >> 3) * 1024 + (r & 7) * 128 + ((w ^ (r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
+                                 :: "r"(dst), "r"(o0), "r"(o1), "r"(o2), "r"(o3) : "memory");
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar_afull + 8 * stage);
+                if (++stage == S) { stage = 0; phase ^= 1; }
+            }
+        }
+        cp_async_wait<0>();
+    } else if (warp >= EP_WARP0) {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quarter
+        int ic = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ic) {
+            int e, row0, nrows, fb;
+            item_rows<GATEUP>(p, item, e, row0, nrows, fb);
+            const int buf = ic & 1;
+            const uint32_t aph = (ic >> 1) & 1;
+            bool ok = tc::mbar_wait(bar_accfull + 8 * buf, aph, abort_flag, p.err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::tc_fence_after();
+            const int ncb = ceil_div(nrows, 32);
+            for (int cb = 0; cb < ncb; ++cb) {
+                uint32_t v[32];
+                tc::tmem_ld_32x32b_x32(tmem_base + buf * 256 + cb * 32 + ((uint32_t)(32 * q) << 16), v);
+                tc::tmem_ld_wait();
+                if (GATEUP) {
+                    const bool lo_half = lane < 16;
+                    const int feat = fb * 64 + 16 * q + (lane & 15);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t send = lo_half ? v[16 + j] : v[j];
+                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        const float g = __uint_as_float(lo_half ? v[j] : recv);
+                        const float u = __uint_as_float(lo_half ? recv : v[16 + j]);
+                        const int col = cb * 32 + (lo_half ? j : 16 + j);
+                        if (col < nrows)
+                            p.out[(size_t)(row0 + col) * p.out_ld + feat] = float_to_bf16_bits(silu(g) * u);
+                    }
+                } else {
+                    const int feat = fb * BM + 32 * q + lane;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = cb * 32 + j;
+                        if (col < nrows) {
+                            float y = __uint_as_float(v[j]);
+                            if (p.row_w) y *= p.row_w[row0 + col];
+                            p.out[(size_t)(row0 + col) * p.out_ld + feat] = float_to_bf16_bits(y);
+                        }
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar_accempty + 8 * buf);
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+    static EncodeFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(ptr);
+    }
+    return fn;
+}
+
+// 2D map over a row-major [rows][cols] array.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr, uint64_t cols,
+              uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+    EncodeFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * esize};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool GATEUP, int S>
+cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
+    TcParams p{};
+    p.E = E;
+    p.d = d;
+    p.f = f;
+    p.R = R;
+    p.K = GATEUP ? d : f;
+    p.NFB = GATEUP ? f / 64 : d / BM;
+    p.wsc = GATEUP ? in.w13_s : in.w2_s;
+    p.wz = GATEUP ? in.w13_z : in.w2_z;
+    p.tiles = in.tiles;
+    p.plan = in.plan;
+    p.out = GATEUP ? in.h : in.y_perm;
+    p.out_ld = GATEUP ? f : d;
+    p.row_w = GATEUP ? nullptr : in.row_w;
+    p.err = in.err;
+
+    const uint64_t rows_w = (uint64_t)E * (GATEUP ? 2 * (uint64_t)f : (uint64_t)d);
+    CUtensorMap map_w, map_x;
+    if (!make_map(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, GATEUP ? in.w13_q : in.w2_q, (uint64_t)p.K / 8,
+                  rows_w, BK / 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    if (!make_map(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, GATEUP ? in.x_perm : in.h, (uint64_t)p.K,
+                  (uint64_t)R, BK, B_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+
+    const size_t smem = tc_smem_bytes(S, p.K);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<GATEUP, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)tc_smem_bytes(S, S == 4 ? 2048 : 8192));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int max_items = tc_max_tiles(R, E) * p.NFB;
+    const int grid = std::max(1, std::min(num_sms(), max_items));
+    tc_grouped_kernel<GATEUP, S><<<grid, THREADS, smem, s>>>(map_w, map_x, p);
+    note_launch();
+    return cudaGetLastError();
+}
+
+constexpr size_t TC_SMEM_LIMIT = 232448;
+
+}  // namespace
+
+int tc_max_tiles(int R, int E) { return ceil_div(R, TILE_ROWS) + std::min(R, E); }
+
+bool tc_supported(int E, int d, int f) {
+    (void)E;
+    if (d % 256 || f % 256) return false;
+    // 4 stages while the scale buffers fit, else 3
+    const int Kmax = std::max(d, f);
+    return tc_smem_bytes(3, Kmax) <= TC_SMEM_LIMIT && d <= 8192 && f <= 8192;
+}
+
+cudaError_t launch_tc_gateup(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    if (tc_smem_bytes(4, d) <= TC_SMEM_LIMIT) return launch_impl<true, 4>(E, d, f, R, in, s);
+    return launch_impl<true, 3>(E, d, f, R, in, s);
+}
+
+cudaError_t launch_tc_down(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    if (tc_smem_bytes(4, f) <= TC_SMEM_LIMIT) return launch_impl<false, 4>(E, d, f, R, in, s);
+    return launch_impl<false, 3>(E, d, f, R, in, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,254 @@
+// Stage 2: token -> expert permutation (stable counting sort) and gather.
+//
+// The assignments a = t*k + j are grouped by expert so that each expert's
+// weights are read once for the whole batch ("Performance and verification",
+// section "Why it is fast").  Inside an expert's segment the assignments keep
+// ascending a (a stable sort), so the permutation is unique and is compared
+// bit-exactly.
+//
+// Small batches (R <= ALIGN_SMALL_MAX_R) use one CTA for everything.  Larger
+// batches use: per-block histograms -> one scan CTA -> per-block stable
+// scatter (one warp walks its block's assignments in order) -> row gather.
+// Besides counts/offsets/sorted/inv the scan also emits the list of experts
+// with rows (for the GEMV regime) and the token tiles (for the tensor-core
+// regime).  An id outside [0, E) sets the range error bit and is skipped.
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int SCAN_THREADS = 1024;
+
+// Exclusive block scan of one int per thread (blockDim.x == SCAN_THREADS).
+// Returns the exclusive prefix; `total` receives the block total.
+__device__ int block_exclusive_scan(int v, int& total) {
+    __shared__ int warp_sums[32];
+    __shared__ int s_total;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += n;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        const int ws = warp_sums[lane];
+        int wincl = ws;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, wincl, off);
+            if (lane >= off) wincl += n;
+        }
+        warp_sums[lane] = wincl - ws;  // exclusive prefix of the warp sums
+        if (lane == 31) s_total = wincl;
+    }
+    __syncthreads();
+    const int res = warp_sums[wid] + incl - v;
+    total = s_total;
+    __syncthreads();  // warp_sums / s_total are reused by the next call
+    return res;
+}
+
+// Per-expert totals -> offsets, counts, uniq list and tiles (one CTA of
+// SCAN_THREADS threads; thread e owns expert e).
+__device__ void emit_plan(int cnt, int e, int E, int32_t* counts, int32_t* offsets, int32_t* uniq,
+                          Tile* tiles, DevPlan* plan, int* s_offset_out) {
+    int total;
+    const bool live = e < E;
+    const int c = live ? cnt : 0;
+    const int off = block_exclusive_scan(c, total);
+    if (live) {
+        if (counts) counts[e] = c;
+        if (offsets) offsets[e] = off;
+    }
+    if (threadIdx.x == 0 && offsets) offsets[E] = total;
+    if (s_offset_out) *s_offset_out = off;
+    // experts with rows, ascending id
+    const int has = (live && c > 0) ? 1 : 0;
+    int n_uniq;
+    const int upos = block_exclusive_scan(has, n_uniq);
+    if (has && uniq) uniq[upos] = e;
+    // token tiles of at most TILE_ROWS rows
+    const int nt = live ? ceil_div(c, TILE_ROWS) : 0;
+    int n_tiles;
+    const int tpos = block_exclusive_scan(nt, n_tiles);
+    if (tiles) {
+        for (int i = 0; i < nt; ++i) {
+            Tile tl;
+            tl.expert = e;
+            tl.row0 = off + i * TILE_ROWS;
+            tl.nrows = min(TILE_ROWS, c - i * TILE_ROWS);
+            tl.pad = 0;
+            tiles[tpos + i] = tl;
+        }
+    }
+    if (threadIdx.x == 0 && plan) {
+        plan->n_uniq = n_uniq;
+        plan->n_tiles = n_tiles;
+    }
+}
+
+// Stable placement of assignments [a0, a1) by one warp, walking them in
+// ascending order 32 at a time.  run[e] holds the next free position of e.
+__device__ void warp_stable_scatter(const int32_t* __restrict__ ids, int a0, int a1, int E, int* run,
+                                    int32_t* __restrict__ sorted, int32_t* __restrict__ inv,
+                                    uint32_t* err) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int base = a0; base < a1; base += 32) {
+        const int a = base + lane;
+        int e = (a < a1) ? ids[a] : -1;
+        const bool valid = (a < a1) && e >= 0 && e < E;
+        if (a < a1 && !valid) set_error(err, ERRBIT_RANGE);
+        const int key = valid ? e : -1;
+        const uint32_t peers = __match_any_sync(0xffffffffu, key);
+        if (valid) {
+            const int rank = __popc(peers & lt);
+            const int pos = run[e] + rank;
+            sorted[pos] = a;
+            inv[a] = pos;
+        }
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) run[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// Copy rows x[sorted[i] / k] -> x_perm[i] for i in [i0, i1), 16 bytes per lane.
+__device__ void gather_rows(const uint16_t* __restrict__ x, int d, int k, const int32_t* __restrict__ sorted,
+                            int i0, int i1, uint16_t* __restrict__ x_perm, int warp, int nwarps) {
+    const int lane = threadIdx.x & 31;
+    const int vec = d / 8;  // 16-byte vectors per row
+    for (int i = i0 + warp; i < i1; i += nwarps) {
+        const int a = sorted[i];
+        if (a < 0 || a >= i1) continue;  // a slot left unwritten by out-of-range ids
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(a / k) * d);
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)i * d);
+        for (int v = lane; v < vec; v += 32) dst[v] = src[v];
+    }
+}
+
+// -------------------------------------------------------------- small path
+__global__ void __launch_bounds__(SCAN_THREADS) align_small_kernel(const int32_t* __restrict__ ids, int R, int k, int E,
+                                                                   const uint16_t* __restrict__ x, int d,
+                                                                   AlignOut o) {
+    __shared__ int cnt[1024];
+    __shared__ int run[1024];
+    const int tid = threadIdx.x;
+    if (tid < E) cnt[tid] = 0;
+    __syncthreads();
+    for (int a = tid; a < R; a += SCAN_THREADS) {
+        const int e = ids[a];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else set_error(o.err, ERRBIT_RANGE);
+    }
+    __syncthreads();
+    int my_off = 0;
+    emit_plan(tid < E ? cnt[tid] : 0, tid, E, o.counts, o.offsets, o.uniq, o.tiles, o.plan, &my_off);
+    if (tid < E) run[tid] = my_off;
+    __syncthreads();
+    if (tid < 32) warp_stable_scatter(ids, 0, R, E, run, o.sorted, o.inv, o.err);
+    if (o.x_perm) {
+        __syncthreads();
+        gather_rows(x, d, k, o.sorted, 0, R, o.x_perm, tid >> 5, SCAN_THREADS / 32);
+    }
+}
+
+// -------------------------------------------------------- multi-block path
+__global__ void __launch_bounds__(256) align_hist_kernel(const int32_t* __restrict__ ids, int R, int E,
+                                                         int32_t* __restrict__ blockcnt, uint32_t* err) {
+    __shared__ int cnt[1024];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int a0 = blockIdx.x * ALIGN_BLOCK_ROWS;
+    const int a1 = min(R, a0 + ALIGN_BLOCK_ROWS);
+    for (int a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
+        const int e = ids[a];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else set_error(err, ERRBIT_RANGE);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// Turns blockcnt[b][e] into the first position of block b's assignments to e.
+__global__ void __launch_bounds__(SCAN_THREADS) align_scan_kernel(int nblocks, int E, int32_t* __restrict__ blockcnt,
+                                                                  AlignOut o) {
+    const int e = threadIdx.x;
+    int total = 0;
+    if (e < E) {
+        for (int b = 0; b < nblocks; ++b) {
+            const int c = blockcnt[(size_t)b * E + e];
+            blockcnt[(size_t)b * E + e] = total;
+            total += c;
+        }
+    }
+    int off = 0;
+    emit_plan(total, e, E, o.counts, o.offsets, o.uniq, o.tiles, o.plan, &off);
+    if (e < E)
+        for (int b = 0; b < nblocks; ++b) blockcnt[(size_t)b * E + e] += off;
+}
+
+__global__ void __launch_bounds__(32) align_scatter_kernel(const int32_t* __restrict__ ids, int R, int E,
+                                                           const int32_t* __restrict__ blockcnt, AlignOut o) {
+    __shared__ int run[1024];
+    for (int e = threadIdx.x; e < E; e += 32) run[e] = blockcnt[(size_t)blockIdx.x * E + e];
+    __syncwarp();
+    const int a0 = blockIdx.x * ALIGN_BLOCK_ROWS;
+    const int a1 = min(R, a0 + ALIGN_BLOCK_ROWS);
+    warp_stable_scatter(ids, a0, a1, E, run, o.sorted, o.inv, o.err);
+}
+
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int d, int k, int R,
+                                                     const int32_t* __restrict__ sorted, uint16_t* __restrict__ x_perm) {
+    const int warps = blockDim.x >> 5;
+    gather_rows(x, d, k, sorted, 0, R, x_perm, blockIdx.x * warps + (threadIdx.x >> 5), gridDim.x * warps);
+}
+
+__global__ void __launch_bounds__(SCAN_THREADS) plan_from_offsets_kernel(const int32_t* __restrict__ offsets, int E,
+                                                                         int32_t* uniq, Tile* tiles, DevPlan* plan) {
+    const int e = threadIdx.x;
+    const int c = (e < E) ? offsets[e + 1] - offsets[e] : 0;
+    emit_plan(c, e, E, nullptr, nullptr, uniq, tiles, plan, nullptr);
+}
+
+}  // namespace
+
+size_t align_blockcnt_bytes(int R, int E) {
+    if (R <= ALIGN_SMALL_MAX_R) return 0;
+    return (size_t)ceil_div(R, ALIGN_BLOCK_ROWS) * E * sizeof(int32_t);
+}
+
+cudaError_t launch_align(const int32_t* ids, int T, int k, int E, const uint16_t* x, int d,
+                         const AlignOut& o, cudaStream_t s) {
+    const int R = T * k;
+    if (R <= ALIGN_SMALL_MAX_R) {
+        align_small_kernel<<<1, SCAN_THREADS, 0, s>>>(ids, R, k, E, x, d, o);
+        note_launch();
+        return cudaGetLastError();
+    }
+    const int nb = ceil_div(R, ALIGN_BLOCK_ROWS);
+    align_hist_kernel<<<nb, 256, 0, s>>>(ids, R, E, o.blockcnt, o.err);
+    note_launch();
+    align_scan_kernel<<<1, SCAN_THREADS, 0, s>>>(nb, E, o.blockcnt, o);
+    note_launch();
+    align_scatter_kernel<<<nb, 32, 0, s>>>(ids, R, E, o.blockcnt, o);
+    note_launch();
+    if (o.x_perm) {
+        const int blocks = min(ceil_div(R, 8), 8 * num_sms());
+        gather_kernel<<<blocks, 256, 0, s>>>(x, d, k, R, o.sorted, o.x_perm);
+        note_launch();
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan_from_offsets(const int32_t* offsets, int E, int32_t* uniq, Tile* tiles,
+                                     DevPlan* plan, cudaStream_t s) {
+    plan_from_offsets_kernel<<<1, SCAN_THREADS, 0, s>>>(offsets, E, uniq, tiles, plan);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,118 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before any launch (no GPU needed).
+
+Every call here that carries made-up pointers is one the library must reject
+during argument checking, so nothing is ever launched with them.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.util import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_w4.h")
+
+OK, INVALID, MISALIGNED, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def M():
+    try:
+        build_lib()
+    except RuntimeError as e:  # pragma: no cover
+        pytest.skip(f"cannot build: {e}")
+    import bit_quantized_expert_moe_gb300 as M
+    return M
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:moe_status_t|size_t|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_route_topk", "moe_permute", "moe_expert_ffn_w4a16", "moe_combine", "moe_layer_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(M):
+    lib = M.lib()
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(M):
+    for code, name in M.STATUS.items():
+        assert M.status_str(code) == name
+    assert "sm_103a" in M.version()
+
+
+FAKE = 0x100000  # 16-byte aligned, never dereferenced (every call below fails validation)
+
+
+def fake_layer(M, E=8, d=256, f=512, group=128, ptr=FAKE):
+    return M.moe_w4_layer(E, d, f, group, ptr, ptr, ptr, ptr, ptr, ptr)
+
+
+def test_workspace_sizes(M):
+    lib = M.lib()
+    L = fake_layer(M)
+    a = lib.moe_layer_workspace_size(ctypes.byref(L), 8, 2)
+    b = lib.moe_layer_workspace_size(ctypes.byref(L), 4096, 2)
+    assert 256 < a < b
+    assert lib.moe_layer_workspace_size(ctypes.byref(fake_layer(M, group=64)), 8, 2) == 0
+    assert lib.moe_permute_workspace_size(8, 2, 8) >= 256
+    assert lib.moe_expert_ffn_workspace_size(ctypes.byref(L), 16) > 256
+
+
+def test_layer_forward_rejects_bad_arguments(M):
+    lib = M.lib()
+    P = FAKE
+    big = 1 << 40
+
+    def call(L, T=8, k=2, x=P, lg=P, out=P, ids=None, ws=P, wsb=big):
+        return lib.moe_layer_forward(ctypes.byref(L), x, lg, T, k, out, ids, ws, wsb, None)
+
+    assert call(fake_layer(M, group=64)) == UNSUPPORTED
+    assert call(fake_layer(M, d=384)) == UNSUPPORTED          # not a multiple of 256
+    assert call(fake_layer(M, f=128 + 256)) == UNSUPPORTED
+    assert call(fake_layer(M, E=0)) == INVALID
+    assert call(fake_layer(M, E=2000)) == INVALID
+    assert call(fake_layer(M, ptr=0)) == INVALID
+    assert call(fake_layer(M, ptr=FAKE + 4)) == MISALIGNED
+    assert call(fake_layer(M), k=9) == INVALID                 # k > E
+    assert call(fake_layer(M), k=0) == INVALID
+    assert call(fake_layer(M), T=-1) == INVALID
+    assert call(fake_layer(M), x=None) == INVALID
+    assert call(fake_layer(M), ws=None) == INVALID
+    assert call(fake_layer(M), x=P + 8) == MISALIGNED
+    assert call(fake_layer(M), ids=P + 2) == MISALIGNED
+    assert call(fake_layer(M), wsb=100) == WORKSPACE
+    assert call(fake_layer(M), T=0) == OK                      # empty batch: no-op, nothing launched
+
+
+def test_stage_entry_points_reject_bad_arguments(M):
+    lib = M.lib()
+    P = FAKE
+    assert lib.moe_route_topk(P, 4, 8, 9, P, P, None) == INVALID
+    assert lib.moe_route_topk(P, 4, 2000, 2, P, P, None) == INVALID
+    assert lib.moe_route_topk(P + 4, 4, 8, 2, P, P, None) == MISALIGNED
+    assert lib.moe_route_topk(None, 4, 8, 2, P, P, None) == INVALID
+    assert lib.moe_route_topk(None, 0, 8, 2, None, None, None) == OK
+    assert lib.moe_permute(P, 4, 9, 8, None, 0, P, P, P, P, None, P, 1 << 30, None) == INVALID
+    assert lib.moe_permute(P, 4, 2, 8, None, 0, P, P, P, P, None, P, 16, None) == WORKSPACE
+    assert lib.moe_permute(P, 4, 2, 8, None, 0, P + 4, P, P, P, None, P, 1 << 30, None) == MISALIGNED
+    assert lib.moe_permute(P, 4, 2, 8, None, 0, P, P, P, P, P, P, 1 << 30, None) == INVALID  # x_perm without x
+    assert lib.moe_combine(P, P, P, 4, 2, 12, P, None) == INVALID   # d % 8
+    assert lib.moe_combine(P, P, P, 4, 0, 16, P, None) == INVALID
+    assert lib.moe_combine(P, P + 4, P, 4, 2, 16, P, None) == MISALIGNED
+    assert lib.moe_combine(None, None, None, 0, 2, 16, None, None) == OK
+    L = fake_layer(M)
+    assert lib.moe_expert_ffn_w4a16(ctypes.byref(L), P, P, 16, None, P, P, 8, None) == WORKSPACE
+    assert lib.moe_expert_ffn_w4a16(ctypes.byref(L), P, None, 16, None, P, P, 1 << 30, None) == INVALID
+    assert lib.moe_expert_ffn_w4a16(ctypes.byref(L), P + 2, P, 16, None, P, P, 1 << 30, None) == MISALIGNED
+    assert lib.moe_get_device_error(None, None) == INVALID
