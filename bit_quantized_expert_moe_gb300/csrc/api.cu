@@ -47,7 +47,9 @@ struct StageMarks {
         }
     }
     void mark(int i) {
-        if (ev) cudaEventRecord(ev[i], s);
+        // external record: inside a stream capture this becomes an event-record
+        // node of the graph, so replays time the stages too
+        if (ev) cudaEventRecordWithFlags(ev[i], s, cudaEventRecordExternal);
     }
 };
 
@@ -113,7 +115,8 @@ struct LayerWs {
     PermScratch ps;
     int32_t *ids, *counts, *offsets, *sorted, *inv;
     float* w;
-    uint16_t *x_perm, *h, *y_perm;
+    float* h;             // fp32 [R][f] (GEMV regime) or fp16 [R][f] (tensor-core regime)
+    uint16_t *x_perm, *y_perm;  // fp16 [R][d] (tensor-core regime)
     size_t bytes;
 };
 
@@ -128,7 +131,7 @@ LayerWs carve_layer(void* ws, int T, int k, int E, int d, int f) {
     l.offsets = c.take<int32_t>(E + 1);
     l.sorted = c.take<int32_t>(R);
     l.inv = c.take<int32_t>(R);
-    l.h = c.take<uint16_t>((size_t)R * f);
+    l.h = c.take<float>((size_t)R * f);
     l.x_perm = c.take<uint16_t>((size_t)R * d);
     l.y_perm = c.take<uint16_t>((size_t)R * d);
     l.bytes = c.off;
@@ -137,15 +140,17 @@ LayerWs carve_layer(void* ws, int T, int k, int E, int d, int f) {
 
 struct FfnWs {
     PermScratch ps;
-    uint16_t* h;
+    float* h;       // fp32 [R][f] (GEMV regime) or fp16 [R][f] (tensor-core regime)
+    uint16_t* x16;  // fp16 copy of x_perm (tensor-core regime)
     size_t bytes;
 };
 
-FfnWs carve_ffn(void* ws, int R, int E, int f) {
+FfnWs carve_ffn(void* ws, int R, int E, int d, int f) {
     Carver c(ws);
     FfnWs w;
     w.ps = carve_perm(c, R, E);
-    w.h = c.take<uint16_t>((size_t)R * f);
+    w.h = c.take<float>((size_t)R * f);
+    w.x16 = c.take<uint16_t>((size_t)R * d);
     w.bytes = c.off;
     return w;
 }
@@ -200,6 +205,7 @@ const char* moe_status_str(moe_status_t s) {
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
         case MOE_ERR_DEVICE_RANGE: return "MOE_ERR_DEVICE_RANGE";
         case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_F16_RANGE: return "MOE_ERR_F16_RANGE";
     }
     return "MOE_ERR_UNKNOWN";
 }
@@ -239,13 +245,13 @@ moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t 
     Carver c(workspace);
     PermScratch s = carve_perm(c, R, E);
     AlignOut o{counts, offsets, sorted, inv, s.uniq, s.tiles, s.plan,
-               static_cast<uint16_t*>(x_perm_bf16), s.blockcnt, err_word(workspace)};
+               static_cast<uint16_t*>(x_perm_bf16), 0, s.blockcnt, err_word(workspace)};
     return cuda_status(launch_align(topk_ids, T, k, E, static_cast<const uint16_t*>(x_bf16), d, o, stream));
 }
 
 size_t moe_expert_ffn_workspace_size(const moe_w4_layer* L, int32_t R) {
     if (check_layer(L) != MOE_OK || R < 0) return 0;
-    return carve_ffn(nullptr, R, L->E, L->d_ff).bytes;
+    return carve_ffn(nullptr, R, L->E, L->d_model, L->d_ff).bytes;
 }
 
 moe_status_t moe_expert_ffn_w4a16(const moe_w4_layer* L, const void* x_perm_bf16, const int32_t* offsets,
@@ -261,7 +267,7 @@ moe_status_t moe_expert_ffn_w4a16(const moe_w4_layer* L, const void* x_perm_bf16
     if (workspace_bytes < moe_expert_ffn_workspace_size(L, R)) return MOE_ERR_WORKSPACE;
     if (R == 0) return MOE_OK;
     const int E = L->E, d = L->d_model, f = L->d_ff;
-    FfnWs w = carve_ffn(workspace, R, E, f);
+    FfnWs w = carve_ffn(workspace, R, E, d, f);
     uint32_t* err = err_word(workspace);
     cudaError_t ce = launch_plan_from_offsets(offsets, E, w.ps.uniq, w.ps.tiles, w.ps.plan, stream);
     if (ce != cudaSuccess) return MOE_ERR_CUDA;
@@ -283,12 +289,15 @@ moe_status_t moe_expert_ffn_w4a16(const moe_w4_layer* L, const void* x_perm_bf16
         return cuda_status(ce);
     }
     if (!tc_supported(E, d, f)) return MOE_ERR_UNSUPPORTED;
+    ce = launch_bf16_to_f16(static_cast<const uint16_t*>(x_perm_bf16), w.x16, (size_t)R * d, err, stream);
+    if (ce != cudaSuccess) return MOE_ERR_CUDA;
     TcIn in = tc_in(L);
     in.tiles = w.ps.tiles;
     in.plan = w.ps.plan;
-    in.x_perm = static_cast<const uint16_t*>(x_perm_bf16);
-    in.h = w.h;
-    in.y_perm = static_cast<uint16_t*>(y_perm_bf16);
+    in.x16 = w.x16;
+    in.h16 = reinterpret_cast<uint16_t*>(w.h);
+    in.y_out = static_cast<uint16_t*>(y_perm_bf16);
+    in.y_f16 = 0;
     in.row_w = row_w;
     in.err = err;
     ce = launch_tc_gateup(E, d, f, R, in, stream);
@@ -304,7 +313,7 @@ moe_status_t moe_combine(const void* y_perm_bf16, const int32_t* inv, const floa
     if (!y_perm_bf16 || !inv || !topk_w || !out_bf16) return MOE_ERR_INVALID_ARG;
     if (!aligned16(y_perm_bf16) || !aligned16(inv) || !aligned16(topk_w) || !aligned16(out_bf16))
         return MOE_ERR_MISALIGNED;
-    return cuda_status(launch_combine(static_cast<const uint16_t*>(y_perm_bf16), inv, topk_w, T, k, d,
+    return cuda_status(launch_combine(static_cast<const uint16_t*>(y_perm_bf16), false, inv, topk_w, T, k, d,
                                       static_cast<uint16_t*>(out_bf16), stream));
 }
 
@@ -341,7 +350,7 @@ moe_status_t moe_layer_forward(const moe_w4_layer* L, const void* x_bf16, const 
     if (ce != cudaSuccess) return MOE_ERR_CUDA;
     marks.mark(1);
     AlignOut o{w.counts, w.offsets, w.sorted, w.inv, w.ps.uniq, w.ps.tiles, w.ps.plan,
-               decode ? nullptr : w.x_perm, w.ps.blockcnt, err};
+               decode ? nullptr : w.x_perm, 1, w.ps.blockcnt, err};
     ce = launch_align(ids, T, k, E, static_cast<const uint16_t*>(x_bf16), d, o, stream);
     if (ce != cudaSuccess) return MOE_ERR_CUDA;
     marks.mark(2);
@@ -371,16 +380,17 @@ moe_status_t moe_layer_forward(const moe_w4_layer* L, const void* x_bf16, const 
     TcIn in = tc_in(L);
     in.tiles = w.ps.tiles;
     in.plan = w.ps.plan;
-    in.x_perm = w.x_perm;
-    in.h = w.h;
-    in.y_perm = w.y_perm;
+    in.x16 = w.x_perm;
+    in.h16 = reinterpret_cast<uint16_t*>(w.h);
+    in.y_out = w.y_perm;
+    in.y_f16 = 1;
     in.row_w = nullptr;
     in.err = err;
     ce = launch_tc_gateup(E, d, f, R, in, stream);
     marks.mark(3);
     if (ce == cudaSuccess) ce = launch_tc_down(E, d, f, R, in, stream);
     marks.mark(4);
-    if (ce == cudaSuccess) ce = launch_combine(w.y_perm, w.inv, w.w, T, k, d, static_cast<uint16_t*>(out_bf16), stream);
+    if (ce == cudaSuccess) ce = launch_combine(w.y_perm, true, w.inv, w.w, T, k, d, static_cast<uint16_t*>(out_bf16), stream);
     marks.mark(5);
     return cuda_status(ce);
 }
@@ -403,7 +413,8 @@ moe_status_t moe_get_device_error(void* workspace, cudaStream_t stream) {
     if (e == 0) return MOE_OK;
     if (cudaMemset(workspace, 0, sizeof(e)) != cudaSuccess) return MOE_ERR_CUDA;
     if (e & ERRBIT_TIMEOUT) return MOE_ERR_TIMEOUT;
-    return MOE_ERR_DEVICE_RANGE;
+    if (e & ERRBIT_RANGE) return MOE_ERR_DEVICE_RANGE;
+    return MOE_ERR_F16_RANGE;
 }
 
 }  // extern "C"

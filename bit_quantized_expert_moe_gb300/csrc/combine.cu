@@ -1,7 +1,8 @@
 // Stage 4: router-weighted combine back to token order.
 //
 // out[t][n] = sum_{j<k} w[t][j] * y_perm[inv[t*k+j]][n], fp32 accumulation in
-// slot order j = 0..k-1, one rounding to bf16 at the end.  Each thread owns
+// slot order j = 0..k-1, one rounding to bf16 at the end.  y_perm is bf16 at
+// the C ABI and fp16 inside the layer (the tensor-core regime's output).  Each thread owns
 // 8 consecutive features of one token (16-byte loads and stores); the grid is
 // a multiple of the SM count and strides over (token, 8-feature chunk).
 #include "internal.h"
@@ -9,6 +10,7 @@
 namespace moe {
 namespace {
 
+template <bool Y_F16>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y_perm,
                                                       const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int T, int k, int d,
@@ -30,8 +32,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
             const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = fmaf(wj, __uint_as_float(u[i] << 16), acc[2 * i]);
-                acc[2 * i + 1] = fmaf(wj, __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                float lo, hi;
+                if (Y_F16) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+                    lo = f.x;
+                    hi = f.y;
+                } else {
+                    lo = __uint_as_float(u[i] << 16);
+                    hi = __uint_as_float(u[i] & 0xFFFF0000u);
+                }
+                acc[2 * i] = fmaf(wj, lo, acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj, hi, acc[2 * i + 1]);
             }
         }
         uint4 o;
@@ -45,13 +56,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 
 }  // namespace
 
-cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv, const float* w, int T, int k,
+cudaError_t launch_combine(const uint16_t* y_perm, bool y_f16, const int32_t* inv, const float* w, int T, int k,
                            int d, uint16_t* out, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const long long work = (long long)T * (d / 8);
     const int per_wave = num_sms() * 8;  // 8 CTAs of 256 threads per SM
     const int blocks = (int)std::min<long long>(per_wave, (work + 255) / 256);
-    combine_kernel<<<blocks, 256, 0, s>>>(y_perm, inv, w, T, k, d, out);
+    if (y_f16)
+        combine_kernel<true><<<blocks, 256, 0, s>>>(y_perm, inv, w, T, k, d, out);
+    else
+        combine_kernel<false><<<blocks, 256, 0, s>>>(y_perm, inv, w, T, k, d, out);
     note_launch();
     return cudaGetLastError();
 }

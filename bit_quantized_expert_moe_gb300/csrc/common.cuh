@@ -19,6 +19,7 @@ namespace moe {
 // ---------------------------------------------------------------------------
 constexpr uint32_t ERRBIT_RANGE = 1u;    // an expert id outside [0, E)
 constexpr uint32_t ERRBIT_TIMEOUT = 2u;  // a bounded pipeline wait gave up
+constexpr uint32_t ERRBIT_F16_RANGE = 4u;  // a value outside the fp16 range of the tensor-core regime
 constexpr size_t WS_HEADER = 256;
 
 struct WsHeader {
@@ -102,6 +103,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Two fp32 -> packed f16x2 (round to nearest even): low half = lo, high half = hi.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// True if either half of a packed f16x2 word is infinite or NaN.
+__device__ __forceinline__ bool f16x2_nonfinite(uint32_t p) {
+    return ((p & 0x7C00u) == 0x7C00u) || ((p & 0x7C000000u) == 0x7C000000u);
+}
+
+__device__ __forceinline__ uint16_t float_to_f16_bits(float v) {
+    return __half_as_ushort(__float2half_rn(v));
 }
 
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float v) {

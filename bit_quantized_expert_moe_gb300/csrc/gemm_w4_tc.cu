@@ -9,16 +9,20 @@
 //
 // Shapes (swap-AB: weight rows are the MMA's M, tokens its N):
 //   D[m][n] = sum_k A[m][k] * B[n][k]     M = 128 weight rows, N <= 256 tokens
-//   A = dequantised weights (bf16, written by the dequant warps, SW128 K-major)
-//   B = activation rows of one expert segment (bf16, TMA, SW128 K-major)
+//   A = dequantised weights (fp16, written by the dequant warps, SW128 K-major)
+//   B = activation rows of one expert segment (fp16, TMA, SW128 K-major)
+// The operands are fp16 rather than bf16: bf16 activations convert to fp16
+// exactly inside fp16's range, and (q - z) * s rounds to fp16 with 8x less
+// error than to bf16; values outside fp16's range set the error word.
 // A work item is (token tile of one expert, block of 128 weight rows); a
 // persistent CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...
 //
 // gate_up: the 128 A rows of a block hold 64 gate rows and the 64 matching up
 // rows, interleaved by 16 inside each 32-lane TMEM quarter, so one thread's
 // lane and the lane 16 above it carry gate and up of the same feature; the
-// epilogue pairs them with one shuffle and writes h = SiLU(g) * u (bf16).
-// down: 128 consecutive rows of W2; the epilogue writes y rows (bf16).
+// epilogue pairs them with one shuffle and writes h = SiLU(g) * u (fp16).
+// down: 128 consecutive rows of W2; the epilogue writes y rows (fp16 for the
+// layer's own combine, bf16 when y is the caller's output).
 //
 // Warp roles (512 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
 // 2-3 idle, 4-11 dequantisation, 12-15 epilogue (TMEM lane quarters 0..3).
@@ -33,7 +37,7 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;                  // A rows per item
-constexpr int BK = 64;                   // K per stage: one 128-byte swizzle row of bf16
+constexpr int BK = 64;                   // K per stage: one 128-byte swizzle row of fp16
 constexpr int BN = TILE_ROWS;            // max tokens per item (256)
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_BYTES = BN * BK * 2;     // 32 KB
@@ -54,8 +58,9 @@ struct TcParams {
     const uint16_t* wz;    // zeros
     const Tile* tiles;
     const DevPlan* plan;
-    uint16_t* out;         // h [R][f] or y [R][d]
+    uint16_t* out;         // h [R][f] (fp16) or y [R][d]
     int out_ld;            // f or d
+    int out_f16;           // down: 1 = fp16 y, 0 = bf16 y
     const float* row_w;
     uint32_t* err;
 };
@@ -202,7 +207,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 int e, row0, nrows, fb;
                 item_rows<GATEUP>(p, item, e, row0, nrows, fb);
                 const int N = ceil_div(nrows, 16) * 16;
-                const uint32_t idesc = tc::idesc_bf16_f32(BM, N);
+                const uint32_t idesc = tc::idesc_f16_f32(BM, N);
                 const int buf = ic & 1;
                 const uint32_t aph = (ic >> 1) & 1;
                 if (!tc::mbar_wait(bar_accempty + 8 * buf, aph ^ 1, abort_flag, p.err)) { ok = false; break; }
@@ -215,7 +220,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                     const uint32_t a0 = sA + stage * A_BYTES, b0 = sB + stage * B_BYTES;
 #pragma unroll
                     for (int ks = 0; ks < BK / 16; ++ks) {
-                        tc::mma_bf16(d_tmem, tc::sw128_kmajor_desc(a0 + ks * 32), tc::sw128_kmajor_desc(b0 + ks * 32),
+                        tc::mma_f16(d_tmem, tc::sw128_kmajor_desc(a0 + ks * 32), tc::sw128_kmajor_desc(b0 + ks * 32),
                                      idesc, (kc | ks) != 0);
                     }
                     tc::mma_commit(bar_empty + 8 * stage);
@@ -299,10 +304,10 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                     const float2 q12 = ffma2(v[1], sc[it], cc[it]);
                     const float2 q56 = ffma2(v[2], sc[it], cc[it]);
                     const float2 q70 = ffma2(v[3], sc[it], cc[it]);
-                    const uint32_t o0 = pack_bf16x2(q70.y, q12.x);  // k0, k1
-                    const uint32_t o1 = pack_bf16x2(q12.y, q34.x);  // k2, k3
-                    const uint32_t o2 = pack_bf16x2(q34.y, q56.x);  // k4, k5
-                    const uint32_t o3 = pack_bf16x2(q56.y, q70.x);  // k6, k7
+                    const uint32_t o0 = pack_f16x2(q70.y, q12.x);  // k0, k1
+                    const uint32_t o1 = pack_f16x2(q12.y, q34.x);  // k2, k3
+                    const uint32_t o2 = pack_f16x2(q34.y, q56.x);  // k4, k5
+                    const uint32_t o3 = pack_f16x2(q56.y, q70.x);  // k6, k7
                     const int r = r_it[it];
                     const uint32_t dst = a0 + (r >> 3) * 1024 + (r & 7) * 128 + ((w ^ (r & 7)) << 4);
                     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
@@ -342,8 +347,11 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                         const float g = __uint_as_float(lo_half ? v[j] : recv);
                         const float u = __uint_as_float(lo_half ? recv : v[16 + j]);
                         const int col = cb * 32 + (lo_half ? j : 16 + j);
-                        if (col < nrows)
-                            p.out[(size_t)(row0 + col) * p.out_ld + feat] = float_to_bf16_bits(silu(g) * u);
+                        if (col < nrows) {
+                            const uint16_t hb = float_to_f16_bits(silu(g) * u);
+                            if ((hb & 0x7C00u) == 0x7C00u) set_error(p.err, ERRBIT_F16_RANGE);
+                            p.out[(size_t)(row0 + col) * p.out_ld + feat] = hb;
+                        }
                     }
                 } else {
                     const int feat = fb * BM + 32 * q + lane;
@@ -353,7 +361,14 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                         if (col < nrows) {
                             float y = __uint_as_float(v[j]);
                             if (p.row_w) y *= p.row_w[row0 + col];
-                            p.out[(size_t)(row0 + col) * p.out_ld + feat] = float_to_bf16_bits(y);
+                            uint16_t yb;
+                            if (p.out_f16) {
+                                yb = float_to_f16_bits(y);
+                                if ((yb & 0x7C00u) == 0x7C00u) set_error(p.err, ERRBIT_F16_RANGE);
+                            } else {
+                                yb = float_to_bf16_bits(y);
+                            }
+                            p.out[(size_t)(row0 + col) * p.out_ld + feat] = yb;
                         }
                     }
                 }
@@ -415,8 +430,9 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
     p.wz = GATEUP ? in.w13_z : in.w2_z;
     p.tiles = in.tiles;
     p.plan = in.plan;
-    p.out = GATEUP ? in.h : in.y_perm;
+    p.out = GATEUP ? in.h16 : in.y_out;
     p.out_ld = GATEUP ? f : d;
+    p.out_f16 = GATEUP ? 1 : in.y_f16;
     p.row_w = GATEUP ? nullptr : in.row_w;
     p.err = in.err;
 
@@ -425,7 +441,7 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
     if (!make_map(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, GATEUP ? in.w13_q : in.w2_q, (uint64_t)p.K / 8,
                   rows_w, BK / 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    if (!make_map(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, GATEUP ? in.x_perm : in.h, (uint64_t)p.K,
+    if (!make_map(&map_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, GATEUP ? in.x16 : in.h16, (uint64_t)p.K,
                   (uint64_t)R, BK, B_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 

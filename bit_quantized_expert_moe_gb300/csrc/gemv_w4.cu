@@ -19,7 +19,7 @@
 //     sum (q - z) s x = s (sum q x - z sum x);
 //   * partial sums of the C chunk-threads of a row are reduced through shared
 //     memory in batches of FB features (8 lanes per output, shuffles).
-// gate_up writes h = SiLU(g) * u in bf16; down either writes y_perm rows or,
+// gate_up writes h = SiLU(g) * u in fp32; down either writes y_perm rows or,
 // because one CTA sees every expert of its feature range, applies the router
 // weights and writes the combined token rows directly (fixed slot order, no
 // atomics).
@@ -42,23 +42,42 @@ struct XSlice {
     float X;         // sum of the 32 activations
 };
 
-__device__ __forceinline__ void load_xslice(const uint16_t* __restrict__ row, int c, bool valid, XSlice& xs) {
-    uint4 q[4];
-    if (valid) {
+// The 32 activations of chunk c of a row: bf16 rows (gate_up input) or fp32
+// rows (the down projection's input h).
+template <typename TIn>
+__device__ __forceinline__ void load_xslice(const TIn* __restrict__ row, int c, bool valid, XSlice& xs) {
+    float xv[32];
+    if (!valid) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) xv[i] = 0.f;
+    } else if (sizeof(TIn) == 2) {
         const uint4* src = reinterpret_cast<const uint4*>(row + 32 * c);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) q[w] = src[w];
-    } else {
+        for (int w = 0; w < 4; ++w) {
+            const uint4 q = src[w];
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int w = 0; w < 4; ++w) q[w] = make_uint4(0, 0, 0, 0);
+            for (int i = 0; i < 4; ++i) {
+                xv[8 * w + 2 * i] = __uint_as_float(u[i] << 16);
+                xv[8 * w + 2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+            }
+        }
+    } else {
+        const float4* src = reinterpret_cast<const float4*>(row + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 q = src[i];
+            xv[4 * i] = q.x;
+            xv[4 * i + 1] = q.y;
+            xv[4 * i + 2] = q.z;
+            xv[4 * i + 3] = q.w;
+        }
     }
     float so = 0.f, se = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        const float x0 = __uint_as_float(q[w].x << 16), x1 = __uint_as_float(q[w].x & 0xFFFF0000u);
-        const float x2 = __uint_as_float(q[w].y << 16), x3 = __uint_as_float(q[w].y & 0xFFFF0000u);
-        const float x4 = __uint_as_float(q[w].z << 16), x5 = __uint_as_float(q[w].z & 0xFFFF0000u);
-        const float x6 = __uint_as_float(q[w].w << 16), x7 = __uint_as_float(q[w].w & 0xFFFF0000u);
+        const float x0 = xv[8 * w], x1 = xv[8 * w + 1], x2 = xv[8 * w + 2], x3 = xv[8 * w + 3];
+        const float x4 = xv[8 * w + 4], x5 = xv[8 * w + 5], x6 = xv[8 * w + 6], x7 = xv[8 * w + 7];
         xs.p[w][0] = make_float2(x3 * 2048.f, x4 * 128.f);
         xs.p[w][1] = make_float2(x1 * 2048.f, x2 * 128.f);
         xs.p[w][2] = make_float2(x5 * 2048.f, x6 * 128.f);
@@ -192,17 +211,18 @@ gemv_w4_kernel(GemvShape sh, GemvIn in, KernelCfg kc) {
             for (int s = 0; s < NT; ++s) {
                 const int r = p0 + s;
                 const bool v = active && r < my_cnt;
-                const uint16_t* row = nullptr;
-                if (v) {
-                    const int i = my_seg + r;
-                    if (GATEUP) {
+                if (GATEUP) {
+                    const uint16_t* row = nullptr;
+                    if (v) {
+                        const int i = my_seg + r;
                         const int src = in.sorted ? in.sorted[i] / in.k : i;
                         row = in.x + (size_t)src * sh.d;
-                    } else {
-                        row = in.h + (size_t)i * sh.f;
                     }
+                    load_xslice(row, c, v, xs[s]);
+                } else {
+                    const float* row = v ? in.h + (size_t)(my_seg + r) * sh.f : nullptr;
+                    load_xslice(row, c, v, xs[s]);
                 }
-                load_xslice(row, c, v, xs[s]);
             }
             const bool loads = active && p0 < my_cnt;
             const size_t ebase = (size_t)my_e * rows_per_expert;
@@ -300,8 +320,7 @@ gemv_w4_kernel(GemvShape sh, GemvIn in, KernelCfg kc) {
                                 const int r = p0 + s;
                                 if (ug + slot < n_uniq && r < s_cnt[slot]) {
                                     const int i = s_seg[slot] + r;
-                                    const float hval = silu(sum) * other;
-                                    in.h[(size_t)i * sh.f + lo + batch0 + f_i] = float_to_bf16_bits(hval);
+                                    in.h[(size_t)i * sh.f + lo + batch0 + f_i] = silu(sum) * other;
                                 }
                             }
                         } else {

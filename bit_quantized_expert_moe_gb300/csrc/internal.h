@@ -34,6 +34,7 @@ struct AlignOut {
     Tile* tiles;        // [R/TILE_ROWS + E]
     DevPlan* plan;      // n_uniq, n_tiles
     uint16_t* x_perm;   // [R][d] or null
+    int x_perm_f16;     // 1: write x_perm as fp16 (values outside fp16 set the error word)
     int32_t* blockcnt;  // [nblocks][E] scratch for the multi-block path
     uint32_t* err;
 };
@@ -43,11 +44,14 @@ size_t align_blockcnt_bytes(int R, int E);
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, const uint16_t* x, int d,
                          const AlignOut& o, cudaStream_t s);
 // uniq list + tile list from an offsets array already on the device.
+// bf16 -> fp16 copy of n elements (n % 8 == 0); out-of-range values set the error word.
+cudaError_t launch_bf16_to_f16(const uint16_t* in, uint16_t* out, size_t n, uint32_t* err, cudaStream_t s);
 cudaError_t launch_plan_from_offsets(const int32_t* offsets, int E, int32_t* uniq, Tile* tiles,
                                      DevPlan* plan, cudaStream_t s);
 
 // ---------------------------------------------------------------- combine
-cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv, const float* w, int T, int k,
+// y_perm is bf16 (y_f16 = false) or fp16 (y_f16 = true).
+cudaError_t launch_combine(const uint16_t* y_perm, bool y_f16, const int32_t* inv, const float* w, int T, int k,
                            int d, uint16_t* out, cudaStream_t s);
 
 // ------------------------------------------------- decode regime (GEMV)
@@ -65,7 +69,7 @@ struct GemvIn {
     const int32_t* sorted;   // gate_up input row i = x[sorted[i] / k] when non-null, else x[i]
     int k;
     const uint16_t* x;       // bf16 [*][d]
-    uint16_t* h;             // bf16 [R][f] (written by gate_up, read by down)
+    float* h;                // fp32 [R][f] (written by gate_up, read by down)
     // down outputs: exactly one of (y_perm) or (out with topk_w, inv, T)
     uint16_t* y_perm;        // bf16 [R][d]
     const float* row_w;      // optional row scale for y_perm
@@ -85,9 +89,10 @@ struct TcIn {
     const uint16_t *w13_s, *w13_z, *w2_s, *w2_z;
     const Tile* tiles;
     const DevPlan* plan;
-    const uint16_t* x_perm;  // bf16 [R][d]
-    uint16_t* h;             // bf16 [R][f]
-    uint16_t* y_perm;        // bf16 [R][d]
+    const uint16_t* x16;     // fp16 [R][d]: permuted activations
+    uint16_t* h16;           // fp16 [R][f]
+    uint16_t* y_out;         // [R][d], fp16 if y_f16 else bf16
+    int y_f16;
     const float* row_w;      // optional
     uint32_t* err;
 };

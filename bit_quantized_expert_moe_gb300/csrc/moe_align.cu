@@ -116,18 +116,45 @@ __device__ void warp_stable_scatter(const int32_t* __restrict__ ids, int a0, int
     }
 }
 
-// Copy rows x[sorted[i] / k] -> x_perm[i] for i in [i0, i1), 16 bytes per lane.
+// bf16x2 -> f16x2 (exact inside fp16's range); sets *bad on overflow.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, bool& bad) {
+    const uint32_t r = pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+    bad |= f16x2_nonfinite(r);
+    return r;
+}
+
+// Copy rows x[sorted[i] / k] -> x_perm[i] for i in [i0, i1), 16 bytes per lane,
+// converting bf16 to fp16 when TO_F16.
+template <bool TO_F16>
 __device__ void gather_rows(const uint16_t* __restrict__ x, int d, int k, const int32_t* __restrict__ sorted,
-                            int i0, int i1, uint16_t* __restrict__ x_perm, int warp, int nwarps) {
+                            int i0, int i1, uint16_t* __restrict__ x_perm, int warp, int nwarps, uint32_t* err) {
     const int lane = threadIdx.x & 31;
     const int vec = d / 8;  // 16-byte vectors per row
+    bool bad = false;
     for (int i = i0 + warp; i < i1; i += nwarps) {
         const int a = sorted[i];
         if (a < 0 || a >= i1) continue;  // a slot left unwritten by out-of-range ids
         const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(a / k) * d);
         uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)i * d);
-        for (int v = lane; v < vec; v += 32) dst[v] = src[v];
+        for (int v = lane; v < vec; v += 32) {
+            uint4 q = src[v];
+            if (TO_F16) {
+                q.x = bf16x2_to_f16x2(q.x, bad);
+                q.y = bf16x2_to_f16x2(q.y, bad);
+                q.z = bf16x2_to_f16x2(q.z, bad);
+                q.w = bf16x2_to_f16x2(q.w, bad);
+            }
+            dst[v] = q;
+        }
     }
+    if (TO_F16 && bad) set_error(err, ERRBIT_F16_RANGE);
+}
+
+__device__ void gather_any(const AlignOut& o, const uint16_t* x, int d, int k, int R, int warp, int nwarps) {
+    if (o.x_perm_f16)
+        gather_rows<true>(x, d, k, o.sorted, 0, R, o.x_perm, warp, nwarps, o.err);
+    else
+        gather_rows<false>(x, d, k, o.sorted, 0, R, o.x_perm, warp, nwarps, o.err);
 }
 
 // -------------------------------------------------------------- small path
@@ -152,7 +179,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) align_small_kernel(const int32_t
     if (tid < 32) warp_stable_scatter(ids, 0, R, E, run, o.sorted, o.inv, o.err);
     if (o.x_perm) {
         __syncthreads();
-        gather_rows(x, d, k, o.sorted, 0, R, o.x_perm, tid >> 5, SCAN_THREADS / 32);
+        gather_any(o, x, d, k, R, tid >> 5, SCAN_THREADS / 32);
     }
 }
 
@@ -201,10 +228,23 @@ __global__ void __launch_bounds__(32) align_scatter_kernel(const int32_t* __rest
     warp_stable_scatter(ids, a0, a1, E, run, o.sorted, o.inv, o.err);
 }
 
-__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int d, int k, int R,
-                                                     const int32_t* __restrict__ sorted, uint16_t* __restrict__ x_perm) {
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int d, int k, int R, AlignOut o) {
     const int warps = blockDim.x >> 5;
-    gather_rows(x, d, k, sorted, 0, R, x_perm, blockIdx.x * warps + (threadIdx.x >> 5), gridDim.x * warps);
+    gather_any(o, x, d, k, R, blockIdx.x * warps + (threadIdx.x >> 5), gridDim.x * warps);
+}
+
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                                          size_t n16, uint32_t* err) {
+    bool bad = false;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
+        uint4 q = in[i];
+        q.x = bf16x2_to_f16x2(q.x, bad);
+        q.y = bf16x2_to_f16x2(q.y, bad);
+        q.z = bf16x2_to_f16x2(q.z, bad);
+        q.w = bf16x2_to_f16x2(q.w, bad);
+        out[i] = q;
+    }
+    if (bad) set_error(err, ERRBIT_F16_RANGE);
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS) plan_from_offsets_kernel(const int32_t* __restrict__ offsets, int E,
@@ -238,9 +278,18 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, const uint16_t
     note_launch();
     if (o.x_perm) {
         const int blocks = min(ceil_div(R, 8), 8 * num_sms());
-        gather_kernel<<<blocks, 256, 0, s>>>(x, d, k, R, o.sorted, o.x_perm);
+        gather_kernel<<<blocks, 256, 0, s>>>(x, d, k, R, o);
         note_launch();
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bf16_to_f16(const uint16_t* in, uint16_t* out, size_t n, uint32_t* err, cudaStream_t s) {
+    const size_t n16 = n / 8;
+    if (n16 == 0) return cudaSuccess;
+    const int blocks = (int)std::min<size_t>((n16 + 255) / 256, (size_t)num_sms() * 8);
+    bf16_to_f16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(in), reinterpret_cast<uint4*>(out), n16, err);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -99,8 +99,8 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 inputs, fp32 accumulation.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, 16-bit inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -134,7 +134,7 @@ __device__ __forceinline__ void tmem_ld_wait() {
 }
 
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
-// swizzle layout: rows of 64 bf16 (128 B), 8-row atoms of 1024 B, atoms
+// swizzle layout: rows of 64 16-bit elements (128 B), 8-row atoms of 1024 B, atoms
 // SBO = 1024 B apart; the leading-byte offset is unused for this layout.
 // Start address must lie in a 1024-byte aligned atom (plus a k offset of
 // 32 B per 16-element MMA step inside the row).
@@ -148,12 +148,12 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16, both
-// K-major, shape M x N (K = 16 per instruction).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B fp16 (format
+// code 0; bf16 would be 1), both K-major, shape M x N (K = 16 per instruction).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4)                              // D format: f32
-         | (1u << 7)                              // A format: bf16
-         | (1u << 10)                             // B format: bf16
+         | (0u << 7)                              // A format: f16
+         | (0u << 10)                             // B format: f16
          | ((uint32_t)(N >> 3) << 17)             // N / 8
          | ((uint32_t)(M >> 4) << 24);            // M / 16
 }

@@ -60,7 +60,8 @@ typedef enum {
     MOE_ERR_WORKSPACE = 4,     /* workspace null or smaller than the *_workspace_size */
     MOE_ERR_CUDA = 5,          /* a CUDA launch or runtime call failed */
     MOE_ERR_DEVICE_RANGE = 6,  /* device side: an expert id was outside [0, E) */
-    MOE_ERR_TIMEOUT = 7        /* device side: a bounded pipeline wait gave up */
+    MOE_ERR_TIMEOUT = 7,       /* device side: a bounded pipeline wait gave up */
+    MOE_ERR_F16_RANGE = 8      /* device side: a value left fp16's range in the tensor-core regime */
 } moe_status_t;
 
 /*
@@ -143,6 +144,11 @@ size_t moe_permute_workspace_size(int32_t T, int32_t k, int32_t E);
  * Experts with no rows are not read.  Two regimes, chosen from R on the host:
  * a CUDA-core GEMV for few rows and a tcgen05 tensor-core grouped GEMM for
  * many (override with the environment variable MOE_W4_REGIME=decode|prefill).
+ * Intermediate precision: the GEMV keeps h in fp32; the tensor-core regime
+ * runs fp16 x fp16 -> fp32 MMAs (activations converted exactly from bf16,
+ * weights (q - z) * s rounded once to fp16, h in fp16), so |x|, |h| and, inside
+ * moe_layer_forward, |y| must stay below 65504 there; a value outside fp16's
+ * range is reported as MOE_ERR_F16_RANGE by moe_get_device_error.
  *
  *   x_perm   device bf16 [R][d_model]
  *   offsets  device int32 [E+1], offsets[0] = 0, offsets[E] = R, non-decreasing
@@ -187,8 +193,9 @@ size_t moe_layer_workspace_size(const moe_w4_layer* L, int32_t T, int32_t k);
 /*
  * Reads and clears the device error word kept at the start of a workspace
  * used by moe_permute, moe_expert_ffn_w4a16 or moe_layer_forward.  Waits for
- * `stream` to finish.  Returns MOE_OK, MOE_ERR_DEVICE_RANGE or MOE_ERR_TIMEOUT
- * (or MOE_ERR_CUDA if the copy fails).
+ * `stream` to finish.  Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_RANGE
+ * or MOE_ERR_F16_RANGE, in that order of precedence (or MOE_ERR_CUDA if the
+ * copy fails).
  */
 moe_status_t moe_get_device_error(void* workspace, cudaStream_t stream);
 
@@ -201,6 +208,8 @@ moe_status_t moe_get_device_error(void* workspace, cudaStream_t stream);
  *   0 start, 1 after routing, 2 after the permutation, 3 after gate_up,
  *   4 after down (the decode regime's down kernel also combines), 5 end.
  * Nothing is recorded once fewer than 6 slots remain.  Pass NULL to stop.
+ * The events are recorded as external events, so a call captured into a CUDA
+ * graph records them on every replay of the graph.
  * `events` and `cursor` are host memory owned by the caller.
  *
  * moe_kernel_launches: number of CUDA kernels this library has launched in
