@@ -61,7 +61,8 @@ typedef enum {
     MOE_ERR_CUDA = 5,          /* a CUDA launch or runtime call failed */
     MOE_ERR_DEVICE_RANGE = 6,  /* device side: an expert id was outside [0, E) */
     MOE_ERR_TIMEOUT = 7,       /* device side: a bounded pipeline wait gave up */
-    MOE_ERR_F16_RANGE = 8      /* device side: a value left fp16's range in the tensor-core regime */
+    MOE_ERR_F16_RANGE = 8,     /* device side: a value left fp16's range in the tensor-core regime */
+    MOE_ERR_SCRATCH_LIMIT = 9  /* moe_permute_noalloc: T*k larger than its fixed scratch allows */
 } moe_status_t;
 
 /*
@@ -129,6 +130,38 @@ moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t k, int32_t 
                          int32_t* sorted, int32_t* inv, void* x_perm_bf16,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 size_t moe_permute_workspace_size(int32_t T, int32_t k, int32_t E);
+
+/*
+ * moe_permute without a workspace, for callers that cannot allocate device
+ * memory.  (No counterpart in the method; this is an interface for callers.)
+ *
+ * Who needs it: a host runtime that reserves all of its device memory at
+ * start-up and refuses allocations afterwards (a fixed-pool serving engine),
+ * code that runs where allocating CUDA calls are not allowed (a host function
+ * enqueued with cudaLaunchHostFunc), or a C program that owns only its input
+ * and output buffers.  Such a caller passes inputs and outputs exactly as for
+ * moe_permute; the scratch lives in a fixed array of
+ * MOE_NOALLOC_SCRATCH_BYTES bytes of device global memory that belongs to the
+ * library image, held by every GPU that loads the library until the process
+ * exits.  Nothing is allocated or freed by this call.
+ *
+ *   - T * k above MOE_NOALLOC_MAX_ROWS returns MOE_ERR_SCRATCH_LIMIT and
+ *     launches nothing.  Other argument errors as for moe_permute.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (the call rewrites every part it reads, so no clearing is needed).
+ *     Calls that overlap on the GPU -- on different streams or from different
+ *     host threads on one device -- race on it and must be serialised.
+ *   - There is no error word to read back: ids outside [0, E) are skipped,
+ *     so the sum of counts falls short of T * k.
+ */
+#define MOE_NOALLOC_MAX_ROWS 32768
+#define MOE_NOALLOC_SCRATCH_BYTES (160 * 1024)
+moe_status_t moe_permute_noalloc(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
+                                 const void* x_bf16, int32_t d, int32_t* counts, int32_t* offsets,
+                                 int32_t* sorted, int32_t* inv, void* x_perm_bf16, cudaStream_t stream);
 
 /*
  * Stage 3 -- grouped expert FFN on the permuted rows.  "Performance and
