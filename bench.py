@@ -145,8 +145,10 @@ class ClockSampler:
 class Workload:
     """Synthetic layers of one configuration, resident on the device."""
 
-    def __init__(self, M, torch, name, device):
+    def __init__(self, M, torch, name, device, layers=None):
         self.cfg_name, self.L = WORKLOADS[name]
+        if layers:
+            self.L = layers
         self.name = name
         cfg = S.CONFIGS[self.cfg_name]
         self.cfg = cfg
@@ -398,10 +400,13 @@ def main():
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="layers per step (default: the workload's own)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_env()
     cfg_name, L = WORKLOADS[args.workload]
+    if args.layers:
+        L = args.layers
     cfg = S.CONFIGS[cfg_name]
     config = {"workload": f"{args.workload}: {cfg.name} layer x{L}, T={cfg.T}, d_model={cfg.d}, d_ff={cfg.f}, "
                           f"E={cfg.E}, top-{cfg.k}, int4 g128 (fp16 scale+zero)",
@@ -474,7 +479,7 @@ def main():
     peaks, peak_src = load_peaks()
     dev = torch.device("cuda", local)
 
-    wl = Workload(M, torch, args.workload, dev)
+    wl = Workload(M, torch, args.workload, dev, layers=args.layers or None)
     config["l2"] = (f"inputs larger than L2 ({wl.weight_bytes / 1e9:.1f} GB of distinct expert weights "
                     f"across the step; no flush needed)")
     res = measure(M, torch, wl, args.steps, args.warmup, rank, world, peaks, peak_src)
