@@ -263,7 +263,26 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
     counts_R = cfg.T * cfg.k
 
     decode_regime = counts_R <= 64
-    if decode_regime:
+    # the one-kernel decode layer: exactly one launch per layer
+    fused = decode_regime and launches_per_step == wl.L
+    if fused:
+        # dominant (only) kernel: the whole layer.  Bytes = the touched experts'
+        # gate_up and down matrices + x, logits, ids and out.  Its duration is
+        # the first stage interval (every later mark is recorded after it).
+        io = cfg.T * cfg.d * 2 * 2 + cfg.T * cfg.E * 4 + cfg.T * cfg.k * 4
+        lay_bytes = np.array([u * (expert_bytes(cfg, "gate_up") + expert_bytes(cfg, "down")) + io for u in uniq],
+                             dtype=np.float64)
+        t_lay = per_layer[:, 0] / 1e3
+        achieved = float(lay_bytes.sum() / t_lay.sum() / 1e9)
+        peak = float(peaks["hbm_gbs"])
+        tr = traffic_for("decode_fused_" + wl.name)
+        roofline = {"bound": "hbm", "kernel": "decode_fused_kernel", "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": (round(tr["dram_bytes_per_launch"]) if tr else None),
+                    "algorithmic_bytes_per_launch": round(float(lay_bytes.mean())),
+                    "avg_launch_us": round(float(t_lay.mean() * 1e6), 2),
+                    "peak_source": peak_src}
+    elif decode_regime:
         # dominant kernel: gate_up GEMV; bytes = touched experts' gate+up rows
         gu_bytes = np.array([u * expert_bytes(cfg, "gate_up") + cfg.T * cfg.d * 2 for u in uniq], dtype=np.float64)
         dn_bytes = np.array([u * expert_bytes(cfg, "down") for u in uniq], dtype=np.float64)

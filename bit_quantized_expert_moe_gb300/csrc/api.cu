@@ -155,6 +155,14 @@ FfnWs carve_ffn(void* ws, int R, int E, int d, int f) {
     return w;
 }
 
+// The decode regime of moe_layer_forward runs as one kernel when the shape
+// allows (MOE_W4_DECODE_KERNEL=split forces the route/permute/GEMV chain).
+bool use_fused(int T, int k, const moe_w4_layer* L) {
+    const char* v = std::getenv("MOE_W4_DECODE_KERNEL");
+    if (v && !std::strcmp(v, "split")) return false;
+    return decode_fused_supported(T, k, L->E, L->d_model, L->d_ff);
+}
+
 bool choose_decode(int R, int T, const moe_w4_layer* L) {
     GemvShape sh{L->E, L->d_model, L->d_ff, R, std::min(R, L->E)};
     const Regime rg = regime_override();
@@ -347,6 +355,14 @@ moe_status_t moe_layer_forward(const moe_w4_layer* L, const void* x_bf16, const 
 
     StageMarks marks(stream);
     marks.mark(0);
+    if (decode && use_fused(T, k, L)) {
+        // one kernel for the whole layer: every later stage mark sits after it
+        FusedIn fi{L, static_cast<const uint16_t*>(x_bf16), logits, T, k, static_cast<uint16_t*>(out_bf16),
+                   topk_ids_out, reinterpret_cast<uint16_t*>(w.h), workspace};
+        const cudaError_t fe = launch_decode_fused(fi, stream);
+        for (int i = 1; i <= 5; ++i) marks.mark(i);
+        return cuda_status(fe);
+    }
     cudaError_t ce = launch_route_topk(logits, T, E, k, ids, w.w, stream);
     if (ce != cudaSuccess) return MOE_ERR_CUDA;
     marks.mark(1);
@@ -412,7 +428,8 @@ moe_status_t moe_get_device_error(void* workspace, cudaStream_t stream) {
     uint32_t e = 0;
     if (cudaMemcpy(&e, workspace, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
     if (e == 0) return MOE_OK;
-    if (cudaMemset(workspace, 0, sizeof(e)) != cudaSuccess) return MOE_ERR_CUDA;
+    // the whole header: a call that gave up may also have left its grid-barrier count behind
+    if (cudaMemset(workspace, 0, WS_HEADER) != cudaSuccess) return MOE_ERR_CUDA;
     if (e & ERRBIT_TIMEOUT) return MOE_ERR_TIMEOUT;
     if (e & ERRBIT_RANGE) return MOE_ERR_DEVICE_RANGE;
     return MOE_ERR_F16_RANGE;

@@ -26,6 +26,9 @@ struct WsHeader {
     uint32_t err;        // OR of ERRBIT_*; cleared by moe_get_device_error
     uint32_t reserved[63];
 };
+// Grid-barrier arrival counter of the one-kernel decode layer: a 64-bit word
+// at this 32-bit word index of the header (its own 64-byte sector).
+constexpr int WS_BAR_COUNT_WORD = 16;
 
 // Small device-side plan written by the permutation kernels (after the header).
 struct DevPlan {

@@ -83,6 +83,22 @@ bool gemv_supported(const GemvShape& sh, int T_tokens);
 cudaError_t launch_gemv_gateup(const GemvShape& sh, const GemvIn& in, cudaStream_t s);
 cudaError_t launch_gemv_down(const GemvShape& sh, const GemvIn& in, cudaStream_t s);
 
+// ------------------------- decode regime: the whole layer in one kernel
+// Routing, gate_up, down and combine of T <= 8 tokens in one cooperative
+// persistent launch (decode_fused.cu).
+struct FusedIn {
+    const moe_w4_layer* L;
+    const uint16_t* x;       // bf16 [T][d]
+    const float* logits;     // fp32 [T][E]
+    int T, k;
+    uint16_t* out;           // bf16 [T][d]
+    int32_t* ids_out;        // [T][k] or null
+    uint16_t* hb;            // fp16 scratch, [T*k][f]
+    void* ws;                // workspace (header: error word and grid-barrier counter)
+};
+bool decode_fused_supported(int T, int k, int E, int d, int f);
+cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s);
+
 // ---------------------------------------------- prefill regime (tcgen05)
 struct TcIn {
     const uint32_t *w13_q, *w2_q;
@@ -100,6 +116,11 @@ bool tc_supported(int E, int d, int f);
 int tc_max_tiles(int R, int E);
 cudaError_t launch_tc_gateup(int E, int d, int f, int R, const TcIn& in, cudaStream_t s);
 cudaError_t launch_tc_down(int E, int d, int f, int R, const TcIn& in, cudaStream_t s);
+
+// 3D tensor map over 32-bit words: dims {d0, d1, d2} (d0 contiguous), byte
+// strides s1 (dim 1) and s2 (dim 2), box {b0, b1, b2}, 128-byte swizzle.
+bool make_tensor_map_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                        uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
 
 // ----------------------------------------------------------- device info
 int num_sms();

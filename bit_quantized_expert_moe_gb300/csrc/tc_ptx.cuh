@@ -46,17 +46,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase of parity `parity` to complete.  On timeout it
 // records ERRBIT_TIMEOUT, raises the CTA abort flag and returns false; a wait
 // that sees the abort flag raised by another role returns false at once.
+// The clock and the abort flag are looked at only every 64 polls: try_wait
+// already suspends the thread for a while when the phase is pending, and a
+// clock read per poll in many spinning warps costs issue slots that the
+// working warps need.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-            *abort_flag = 1;
-            set_error(err, ERRBIT_TIMEOUT);
-            return false;
+        if ((it & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                set_error(err, ERRBIT_TIMEOUT);
+                return false;
+            }
         }
     }
 }
@@ -74,6 +80,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];"
         :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y) : "memory");
+}
+
+// 3D tiled load of box at (x, y, z) into shared memory, completing the box's
+// bytes of transaction count on mbarrier `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z) : "memory");
+}
+
+// Arrive on `bar` once every cp.async issued so far by this thread has landed
+// (the arrival is not pre-counted: the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (tensor core).

@@ -38,6 +38,21 @@ def regime():
     set_(old)
 
 
+@pytest.fixture
+def decode_kernel():
+    """Force the decode-regime layer kernel for one test: "fused" (one kernel
+    for the whole layer) or "split" (routing/permutation + two GEMV kernels)."""
+    old = os.environ.get("MOE_W4_DECODE_KERNEL")
+
+    def set_(v):
+        if v is None:
+            os.environ.pop("MOE_W4_DECODE_KERNEL", None)
+        else:
+            os.environ["MOE_W4_DECODE_KERNEL"] = v
+    yield set_
+    set_(old)
+
+
 def _getter(W):
     return lambda e: {key: v[e] for key, v in W.items()}
 
@@ -290,3 +305,69 @@ def test_zero_tokens_is_a_no_op(M):
     lg = torch.empty((0, cfg.E), dtype=torch.float32, device="cuda")
     out = M.layer_forward(layer, x, lg, cfg.k, out=torch.empty((0, cfg.d), dtype=torch.bfloat16, device="cuda"))
     assert out.shape == (0, cfg.d)
+
+
+# ------------------------------------------- decode regime: one-kernel layer
+@pytest.mark.parametrize("kernel", ["fused", "split"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "large_decode"])
+def test_decode_layer_kernels_match_oracle(M, decode_kernel, kernel, name):
+    cfg = S.CONFIGS[name]
+    decode_kernel(kernel)
+    W, x, lg, ids, out = _run_layer(M, cfg)
+    decode_kernel(None)
+    ref, inter = OM.layer_forward(x, lg, _getter(W), cfg.E, cfg.d, cfg.f, cfg.k, want_intermediates=True)
+    assert np.array_equal(ids, inter["ids"])
+    assert_close(out, ref, f"{name} {kernel}")
+
+
+@pytest.mark.parametrize("T,E,k,d,f,ties", [
+    (1, 1, 1, 256, 256, False),     # one expert, one token
+    (3, 4, 4, 256, 512, False),     # every token on every expert
+    (8, 8, 8, 512, 256, False),     # 8 tokens per expert: all MMA columns used
+    (8, 16, 8, 1280, 768, True),    # ragged chunks (10 and 6 groups), tied logits
+    (2, 1024, 32, 256, 256, False), # E = 1024, R = 64
+    (5, 64, 2, 2048, 1024, True),
+])
+def test_fused_decode_layer_shapes(M, T, E, k, d, f, ties):
+    import torch
+    cfg = S.custom("fused", T=T, d=d, f=f, E=E, k=k, cfg_id=70 + T + k)
+    W = S.layer_weights(cfg, 0)
+    _layer_cache.clear()
+    layer = M.Layer.from_numpy(W)
+    x = S.activations(cfg)
+    lg = S.router_logits(cfg)
+    if ties:
+        lg = np.round(lg * 2.0).astype(np.float32) / 2.0  # many equal logits
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    call = M.LayerCall(layer, T, k)
+    out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    call(x_to_dev(x), f32_to_dev(lg), out, ids)
+    assert M.get_device_error(call.ws) == 0
+    ref, inter = OM.layer_forward(x, lg, _getter(W), E, d, f, k, want_intermediates=True)
+    assert np.array_equal(ids.cpu().numpy(), inter["ids"])
+    assert_close(bf16_to_f64(out), ref, f"fused {T},{E},{k},{d},{f}")
+
+
+def test_fused_decode_repeated_calls_share_the_grid_barrier(M):
+    """The one-kernel layer's grid barrier counts arrivals in the workspace
+    header; every call must add exactly one arrival per CTA and leave nothing
+    pending, so calls on one workspace keep working and agree."""
+    import torch
+    cfg = S.CONFIGS["decode"]
+    W = _layer(cfg)
+    layer = M.Layer.from_numpy(W)
+    call = M.LayerCall(layer, cfg.T, cfg.k)
+    outs = []
+    for layer_idx in (0, 1, 0, 1, 0):
+        x = x_to_dev(S.activations(cfg, layer_idx))
+        lg = f32_to_dev(S.router_logits(cfg, layer_idx))
+        o = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+        call(x, lg, o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert M.get_device_error(call.ws) == 0
+    arrivals = int(call.ws[64:72].view(torch.int64).item())
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert arrivals == 5 * n_sm
+    for a, b in ((0, 2), (0, 4), (1, 3)):
+        assert torch.equal(outs[a].view(torch.int16), outs[b].view(torch.int16))
