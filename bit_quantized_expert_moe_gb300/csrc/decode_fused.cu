@@ -85,7 +85,7 @@ struct Tab {
     int32_t ucnt[MAX_R];
     int32_t n_uniq;
     int32_t abort;
-    int32_t pad[30];
+    uint32_t slot_q[32];   // chunk each ring slot holds (set by the producer)
 };
 
 struct Params {
@@ -136,6 +136,14 @@ __device__ __forceinline__ uint64_t atom_add_release_gpu(unsigned long long* p, 
     uint64_t old;
     asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
     return old;
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" :: "r"(smem_u32(p)), "r"(v) : "memory");
 }
 __device__ __forceinline__ void bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
@@ -298,6 +306,30 @@ __device__ __forceinline__ void tile_group(float (&acc)[4], uint32_t sa, int gl,
     acc[3] = fmaf(s1, (da[3] + db[3]) - fmaf(z1, cb.y, cb.x), acc[3]);
 }
 
+// Waits until ring slot `slot` holds chunk q and its data have landed.  The
+// pairs consume different chunks, so a pair may ask for round r of a slot
+// while round r-1 of that slot is still pending; an mbarrier parity wait
+// cannot tell round r from round r-2, so the pair first waits (bounded) until
+// the producer has published q for the slot -- which it does only after round
+// r-1 was consumed -- and only then waits on the full barrier's parity.
+__device__ __forceinline__ bool wait_chunk(Tab& tab, int slot, uint32_t q, uint32_t full, uint32_t parity,
+                                           volatile int* abort_flag, uint32_t* err) {
+    if (ld_acquire_cta(&tab.slot_q[slot]) != q) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1; ld_acquire_cta(&tab.slot_q[slot]) != q; ++it) {
+            if ((it & 63u) == 0) {
+                if (*abort_flag) return false;
+                if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                    *abort_flag = 1;
+                    set_error(err, ERRBIT_TIMEOUT);
+                    return false;
+                }
+            }
+        }
+    }
+    return tc::mbar_wait(full, parity, abort_flag, err);
+}
+
 // ------------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(NTHREADS, 1)
 decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_constant__ CUtensorMap map2,
@@ -317,6 +349,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
 
     // ------------------------------------------------ phase 0: init, routing
     if (threadIdx.x == 0) tab.abort = 0;
+    if (threadIdx.x < 32) tab.slot_q[threadIdx.x] = 0xFFFFFFFFu;
     if (warp == PRODUCER_WARP && lane == 0) {
         for (int i = 0; i < nslot; ++i) {
             tc::mbar_init(full0 + 8u * i, FULL_ARRIVALS);
@@ -430,9 +463,17 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             const int slot = (int)(q % (uint32_t)nslot);
             const uint32_t round = q / (uint32_t)nslot;
             const uint32_t full = full0 + 8u * slot, empty = empty0 + 8u * slot;
-            if (round > 0 && !tc::mbar_wait(empty, (round - 1) & 1u, abort_flag, p.err)) {
-                ok = false;
-                return;
+            if (round > 0) {
+                // one lane waits and the warp follows its verdict; __syncwarp orders
+                // the consumers' last reads of the slot before any lane's new copies
+                int w = 1;
+                if (lane == 0) w = tc::mbar_wait(empty, (round - 1) & 1u, abort_flag, p.err);
+                w = __shfl_sync(0xffffffffu, w, 0);
+                __syncwarp();
+                if (!w) {
+                    ok = false;
+                    return;
+                }
             }
             const uint32_t dst = sbase + (uint32_t)slot * SLOT_BYTES;
             if (lane == 0) {
@@ -449,6 +490,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             const uint32_t sdst = dst + SLOT_CODE + (uint32_t)(arr * SZ_ARRAY + r * 16);
             for (int i = 0; i < (gcv >> 1); ++i) cp_async4(sdst + 4u * i, src + 2 * i);
             tc::cp_async_mbar_arrive_noinc(full);
+            __syncwarp();
+            if (lane == 0) st_release_cta(&tab.slot_q[slot], q);
             ++q;
         };
         for (int tl = 0; tl < n1 && ok; ++tl) {
@@ -516,7 +559,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         for (int c = 0; c < nch1; ++c) {
             const uint32_t q = (uint32_t)(tl * nch1 + c);
             const int slot = (int)(q % (uint32_t)nslot);
-            const bool ready = tc::mbar_wait(full0 + 8u * slot, (q / (uint32_t)nslot) & 1u, abort_flag, p.err);
+            const bool ready =
+                wait_chunk(tab, slot, q, full0 + 8u * slot, (q / (uint32_t)nslot) & 1u, abort_flag, p.err);
             if (ready) {
                 const int gcv = min(CHUNK_GROUPS, Gd - c * CHUNK_GROUPS);
                 const int gb = half * (gcv >> 1), ge = gb + (gcv >> 1);
@@ -626,7 +670,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
                 const uint32_t q = qbase + (uint32_t)(i2 * nch2 + c);
                 const int slot = (int)(q % (uint32_t)nslot);
                 const bool ready =
-                    tc::mbar_wait(full0 + 8u * slot, (q / (uint32_t)nslot) & 1u, abort_flag, p.err);
+                    wait_chunk(tab, slot, q, full0 + 8u * slot, (q / (uint32_t)nslot) & 1u, abort_flag, p.err);
                 if (ready) {
                     const int gcv = min(CHUNK_GROUPS, Gf - c * CHUNK_GROUPS);
                     const int gb = half * (gcv >> 1), ge = gb + (gcv >> 1);
