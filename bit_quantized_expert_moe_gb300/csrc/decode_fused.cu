@@ -38,10 +38,12 @@
 //     C1 = 1024 * sum(x over even k) + 64 * sum(x over odd k),   C2 = sum(x),
 // with C1 and C2 computed once per (token, group) from the same fp16 values.
 //
-// Pipeline.  Warp 16 is the producer: lane 0 issues 3D TMA boxes of the packed
-// codes (16 rows x 4 lines of 128 B = 2 groups each, 128-byte swizzle) into a
-// ring of slots and all its lanes copy the matching fp16 scales and zeros with
-// 4-byte cp.async, tracked by the slot's full mbarrier.  Warps 0..15 form 8
+// Pipeline.  Warps 16..19 are producers (chunk q belongs to warp 16 + q % 4,
+// since issuing one chunk keeps a warp busy for about a thousand cycles):
+// lane 0 issues 3D TMA boxes of the packed codes (16 rows x 4 lines of 128 B =
+// 2 groups each, 128-byte swizzle) into a ring of slots and all lanes copy
+// the matching fp16 scales and zeros with 4-byte cp.async, tracked by the
+// chunk's full mbarrier.  Warps 0..15 form 8
 // pairs; a tile belongs to one pair and each warp of the pair takes half of
 // every chunk's groups; the two halves are added through shared memory.
 // Every wait is bounded (2 s), after which the kernel records a timeout in the
@@ -59,8 +61,9 @@ using tc::WAIT_LIMIT_NS;
 
 constexpr int CW = 16;                          // consumer warps
 constexpr int NPAIR = CW / 2;
-constexpr int PRODUCER_WARP = CW;
-constexpr int NTHREADS = 32 * (CW + 1);
+constexpr int PRODUCER_WARP = CW;               // first producer warp
+constexpr int NPROD = 4;                        // producer warps: chunk q is issued by warp q % NPROD
+constexpr int NTHREADS = 32 * (CW + NPROD);
 constexpr int CONSUMER_THREADS = 32 * CW;
 constexpr int LINES = 4;                        // 128-byte lines (2 groups each) per chunk row
 constexpr int CHUNK_GROUPS = 2 * LINES;         // groups of 128 codes per chunk
@@ -69,6 +72,14 @@ constexpr int SLOT_CODE = 2 * BOX_BYTES;        // 16 rows of codes
 constexpr int SZ_ARRAY = 16 * CHUNK_GROUPS * 2; // fp16 [16 rows][8 groups]
 constexpr int SLOT_BYTES = SLOT_CODE + 1024;    // codes + scales + zeros, 1024-byte aligned
 constexpr uint32_t FULL_ARRIVALS = 1 + 32;      // expect_tx arrival + 32 cp.async arrivals
+// "Full" barriers are indexed by chunk number modulo NFULL, not by ring slot:
+// the pairs consume different chunks, so a pair may wait for chunk q before
+// the chunk that last used q's ring slot has been consumed.  A pair runs at
+// most NPAIR tiles ahead of the chunks already issued, so with
+// NFULL >= nslot + NPAIR * (chunks per tile) + 1 the previous use of q's
+// barrier (chunk q - NFULL) has always landed when q is waited on, and the
+// barrier's parity names q's phase unambiguously.
+constexpr int NFULL = 256;
 constexpr int MAX_T = 8;
 constexpr int MAX_R = 64;
 constexpr int ROW_PAD = 64;                     // bytes after each staged activation row
@@ -85,7 +96,7 @@ struct Tab {
     int32_t ucnt[MAX_R];
     int32_t n_uniq;
     int32_t abort;
-    uint32_t slot_q[32];   // chunk each ring slot holds (set by the producer)
+    int32_t pad[30];
 };
 
 struct Params {
@@ -136,14 +147,6 @@ __device__ __forceinline__ uint64_t atom_add_release_gpu(unsigned long long* p, 
     uint64_t old;
     asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
     return old;
-}
-__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" :: "r"(smem_u32(p)), "r"(v) : "memory");
 }
 __device__ __forceinline__ void bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
@@ -306,30 +309,6 @@ __device__ __forceinline__ void tile_group(float (&acc)[4], uint32_t sa, int gl,
     acc[3] = fmaf(s1, (da[3] + db[3]) - fmaf(z1, cb.y, cb.x), acc[3]);
 }
 
-// Waits until ring slot `slot` holds chunk q and its data have landed.  The
-// pairs consume different chunks, so a pair may ask for round r of a slot
-// while round r-1 of that slot is still pending; an mbarrier parity wait
-// cannot tell round r from round r-2, so the pair first waits (bounded) until
-// the producer has published q for the slot -- which it does only after round
-// r-1 was consumed -- and only then waits on the full barrier's parity.
-__device__ __forceinline__ bool wait_chunk(Tab& tab, int slot, uint32_t q, uint32_t full, uint32_t parity,
-                                           volatile int* abort_flag, uint32_t* err) {
-    if (ld_acquire_cta(&tab.slot_q[slot]) != q) {
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t it = 1; ld_acquire_cta(&tab.slot_q[slot]) != q; ++it) {
-            if ((it & 63u) == 0) {
-                if (*abort_flag) return false;
-                if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-                    *abort_flag = 1;
-                    set_error(err, ERRBIT_TIMEOUT);
-                    return false;
-                }
-            }
-        }
-    }
-    return tc::mbar_wait(full, parity, abort_flag, err);
-}
-
 // ------------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(NTHREADS, 1)
 decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_constant__ CUtensorMap map2,
@@ -340,7 +319,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     Tab& tab = *reinterpret_cast<Tab*>(sm + p.off_tab);
     volatile int* abort_flag = &tab.abort;
     const uint32_t full0 = sbase + p.off_bars;
-    const uint32_t empty0 = full0 + 8u * p.nslot;
+    const uint32_t empty0 = full0 + 8u * NFULL;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = p.T, k = p.k, R = T * k, E = p.E, d = p.d, f = p.f;
     const int Gd = d >> 7, Gf = f >> 7;
@@ -349,12 +328,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
 
     // ------------------------------------------------ phase 0: init, routing
     if (threadIdx.x == 0) tab.abort = 0;
-    if (threadIdx.x < 32) tab.slot_q[threadIdx.x] = 0xFFFFFFFFu;
     if (warp == PRODUCER_WARP && lane == 0) {
-        for (int i = 0; i < nslot; ++i) {
-            tc::mbar_init(full0 + 8u * i, FULL_ARRIVALS);
-            tc::mbar_init(empty0 + 8u * i, 2);
-        }
+        for (int i = 0; i < NFULL; ++i) tc::mbar_init(full0 + 8u * i, FULL_ARRIVALS);
+        for (int i = 0; i < nslot; ++i) tc::mbar_init(empty0 + 8u * i, 2);
         tc::fence_mbar_init();
         tc::tma_prefetch_desc(&map13);
         tc::tma_prefetch_desc(&map2);
@@ -454,15 +430,20 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     const int n1 = b1 - a1, n2u = b2 - a2, n2t = n2u * k;
     const int nch1 = ceil_div(Gd, CHUNK_GROUPS), nch2 = ceil_div(Gf, CHUNK_GROUPS);
 
-    // ---------------------------------------------------------- producer
-    if (warp == PRODUCER_WARP) {
+    // ---------------------------------------------------------- producers
+    if (warp >= PRODUCER_WARP) {
+        const uint32_t pw = (uint32_t)(warp - PRODUCER_WARP);
         uint32_t q = 0;
         bool ok = true;
         auto issue = [&](const CUtensorMap* map, int row0, int row1, int chunk, const uint16_t* s_arr,
                          const uint16_t* z_arr, int Gk) {
+            if (q % NPROD != pw) {  // another producer warp's chunk
+                ++q;
+                return;
+            }
             const int slot = (int)(q % (uint32_t)nslot);
             const uint32_t round = q / (uint32_t)nslot;
-            const uint32_t full = full0 + 8u * slot, empty = empty0 + 8u * slot;
+            const uint32_t full = full0 + 8u * (q % NFULL), empty = empty0 + 8u * slot;
             if (round > 0) {
                 // one lane waits and the warp follows its verdict; __syncwarp orders
                 // the consumers' last reads of the slot before any lane's new copies
@@ -490,8 +471,6 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             const uint32_t sdst = dst + SLOT_CODE + (uint32_t)(arr * SZ_ARRAY + r * 16);
             for (int i = 0; i < (gcv >> 1); ++i) cp_async4(sdst + 4u * i, src + 2 * i);
             tc::cp_async_mbar_arrive_noinc(full);
-            __syncwarp();
-            if (lane == 0) st_release_cta(&tab.slot_q[slot], q);
             ++q;
         };
         for (int tl = 0; tl < n1 && ok; ++tl) {
@@ -508,11 +487,13 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             for (int c = 0; c < nch2 && ok; ++c) issue(&map2, rg, rg + 8, c, p.w2_s, p.w2_z, Gf);
         }
         // drain: the last use of every slot must have landed before the CTA exits
+        // (each warp waits for its own chunks among the last nslot)
         const uint32_t issued = q;
         const uint32_t first = issued > (uint32_t)nslot ? issued - (uint32_t)nslot : 0u;
         for (uint32_t qq = first; qq < issued; ++qq) {
-            const uint32_t full = full0 + 8u * (qq % (uint32_t)nslot);
-            const uint32_t par = (qq / (uint32_t)nslot) & 1u;
+            if (qq % NPROD != pw) continue;
+            const uint32_t full = full0 + 8u * (qq % NFULL);
+            const uint32_t par = (qq / NFULL) & 1u;
             if (tc::mbar_try_wait(full, par)) continue;
             const uint64_t t0 = globaltimer_ns();
             while (!tc::mbar_try_wait(full, par)) {
@@ -559,8 +540,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         for (int c = 0; c < nch1; ++c) {
             const uint32_t q = (uint32_t)(tl * nch1 + c);
             const int slot = (int)(q % (uint32_t)nslot);
-            const bool ready =
-                wait_chunk(tab, slot, q, full0 + 8u * slot, (q / (uint32_t)nslot) & 1u, abort_flag, p.err);
+            const bool ready = tc::mbar_wait(full0 + 8u * (q % NFULL), (q / NFULL) & 1u, abort_flag, p.err);
             if (ready) {
                 const int gcv = min(CHUNK_GROUPS, Gd - c * CHUNK_GROUPS);
                 const int gb = half * (gcv >> 1), ge = gb + (gcv >> 1);
@@ -670,7 +650,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
                 const uint32_t q = qbase + (uint32_t)(i2 * nch2 + c);
                 const int slot = (int)(q % (uint32_t)nslot);
                 const bool ready =
-                    wait_chunk(tab, slot, q, full0 + 8u * slot, (q / (uint32_t)nslot) & 1u, abort_flag, p.err);
+                    tc::mbar_wait(full0 + 8u * (q % NFULL), (q / NFULL) & 1u, abort_flag, p.err);
                 if (ready) {
                     const int gcv = min(CHUNK_GROUPS, Gf - c * CHUNK_GROUPS);
                     const int gb = half * (gcv >> 1), ge = gb + (gcv >> 1);
@@ -731,12 +711,14 @@ bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
     const uint32_t o_tab = take(sizeof(Tab));
     if (fixed + 1024 >= SMEM_LIMIT) return false;
     const size_t avail = SMEM_LIMIT - 1024 - fixed;
-    int nslot = (int)(avail / (SLOT_BYTES + 16));
+    int nslot = (int)((avail - 8 * NFULL) / (SLOT_BYTES + 8));
     nslot = std::min(nslot, 32);
     if (nslot < MIN_SLOTS) return false;
+    const int nch_max = ceil_div(std::max(d, f) / 128, CHUNK_GROUPS);
+    if (nslot + NPAIR * nch_max + 1 > NFULL) return false;
     if ((size_t)T * E * 4 > (size_t)nslot * SLOT_BYTES) return false;  // logits staging
     const uint32_t ring = (uint32_t)nslot * SLOT_BYTES;
-    const uint32_t bars = (uint32_t)align_up((size_t)16 * nslot, 128);
+    const uint32_t bars = (uint32_t)align_up((size_t)8 * (NFULL + nslot), 128);
     l.nslot = nslot;
     l.off_bars = ring;
     l.off_xb = ring + bars + o_xb;

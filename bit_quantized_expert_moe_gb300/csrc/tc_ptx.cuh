@@ -46,17 +46,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase of parity `parity` to complete.  On timeout it
 // records ERRBIT_TIMEOUT, raises the CTA abort flag and returns false; a wait
 // that sees the abort flag raised by another role returns false at once.
-// The clock and the abort flag are looked at only every 64 polls: try_wait
-// already suspends the thread for a while when the phase is pending, and a
-// clock read per poll in many spinning warps costs issue slots that the
-// working warps need.
+// try_wait with a suspend-time hint: while the phase is pending the thread
+// sleeps (up to `ns`) instead of re-polling, so waiting warps leave the
+// shared-memory pipe to the warps that are working.
+constexpr uint32_t WAIT_SUSPEND_NS = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(WAIT_SUSPEND_NS) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity` to complete.  On timeout it
+// records ERRBIT_TIMEOUT, raises the CTA abort flag and returns false; a wait
+// that sees the abort flag raised by another role returns false soon after.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if ((it & 7u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
                 *abort_flag = 1;
