@@ -267,12 +267,13 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
     fused = decode_regime and launches_per_step == wl.L
     if fused:
         # dominant (only) kernel: the whole layer.  Bytes = the touched experts'
-        # gate_up and down matrices + x, logits, ids and out.  Its duration is
-        # the first stage interval (every later mark is recorded after it).
+        # gate_up and down matrices + x, logits, ids and out.  Its average launch
+        # duration comes from the timed region itself, which holds exactly L
+        # back-to-back launches per step (CUDA events on the launching stream).
         io = cfg.T * cfg.d * 2 * 2 + cfg.T * cfg.E * 4 + cfg.T * cfg.k * 4
         lay_bytes = np.array([u * (expert_bytes(cfg, "gate_up") + expert_bytes(cfg, "down")) + io for u in uniq],
                              dtype=np.float64)
-        t_lay = per_layer[:, 0] / 1e3
+        t_lay = np.full(wl.L, ms / wl.L / 1e3)
         achieved = float(lay_bytes.sum() / t_lay.sum() / 1e9)
         peak = float(peaks["hbm_gbs"])
         tr = traffic_for("decode_fused_" + wl.name)

@@ -63,6 +63,7 @@ constexpr int CW = 16;                          // consumer warps
 constexpr int NPAIR = CW / 2;
 constexpr int PRODUCER_WARP = CW;               // first producer warp
 constexpr int NPROD = 4;                        // producer warps: chunk q is issued by warp q % NPROD
+static_assert((NPROD & (NPROD - 1)) == 0, "NPROD must be a power of two");
 constexpr int NTHREADS = 32 * (CW + NPROD);
 constexpr int CONSUMER_THREADS = 32 * CW;
 constexpr int LINES = 4;                        // 128-byte lines (2 groups each) per chunk row
@@ -80,6 +81,7 @@ constexpr uint32_t FULL_ARRIVALS = 1 + 32;      // expect_tx arrival + 32 cp.asy
 // barrier (chunk q - NFULL) has always landed when q is waited on, and the
 // barrier's parity names q's phase unambiguously.
 constexpr int NFULL = 256;
+static_assert((NFULL & (NFULL - 1)) == 0, "NFULL must be a power of two");
 constexpr int MAX_T = 8;
 constexpr int MAX_R = 64;
 constexpr int ROW_PAD = 64;                     // bytes after each staged activation row
@@ -111,6 +113,7 @@ struct Params {
     int T, k, E, d, f;
     int nslot;
     uint32_t off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab;
+    uint32_t off_cnt;          // phase-0 counters inside the ring, after the logits
     int xb_stride, hs_stride;  // bytes per staged row
 };
 
@@ -171,53 +174,76 @@ __device__ __forceinline__ uint32_t route_key(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Top-k of one token whose logits are in shared memory (`row`), by one warp:
-// k rounds of (warp maximum of the keys, then the lowest expert id among the
-// lanes holding it), i.e. a sort by (-logit, id) on the exact fp32 values
-// (router ids must match exactly: "Performance and verification", section
-// "How it is verified").  Weights: softmax over the k selected logits, fp32.
-// The round body has no data-dependent branch (selects only), so the warp
-// stays converged between its warp-wide reductions.
-__device__ void route_token_smem(const float* row, int E, int k, int32_t* out_ids, float* out_w) {
+// Top-k of one token by one warp, logits read once from shared memory (`row`)
+// into registers (VPL per lane: experts lane, lane+32, ...): k rounds of
+// (warp maximum of the keys, then the lowest expert id among the lanes
+// holding it), i.e. a sort by (-logit, id) on the exact fp32 values (router
+// ids must match exactly: "Performance and verification", section "How it is
+// verified").  Lane j (and j+32) keeps slot j; the weights are the softmax of
+// the k <= 64 selected logits, in fp32.  No shared-memory traffic and no
+// data-dependent branch inside the rounds.
+template <int VPL>
+__device__ __forceinline__ void route_token_regs(const float* row, int E, int k, int32_t* out_ids, float* out_w) {
     const int lane = threadIdx.x & 31;
-    const int nv = (E + 31) >> 5;
-    uint32_t taken = 0;
-    float vmax = 0.f;
-    __syncwarp();
+    uint32_t key[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < E ? route_key(row[e]) : 0u;
+    }
+    float vmax = 0.f, v0 = 0.f, v1 = 0.f;
+    int id0 = 0, id1 = 0;
     for (int j = 0; j < k; ++j) {
-        uint32_t bk = 0;
-        int be = INT_MAX;
-        for (int i = 0; i < nv; ++i) {
-            const int e = lane + 32 * i;
-            const bool live = (e < E) & !((taken >> i) & 1u);
-            const uint32_t key = live ? route_key(row[min(e, E - 1)]) : 0u;
-            const bool better = key > bk;  // ascending e: ties keep the lower id
-            bk = better ? key : bk;
-            be = better ? e : be;
+        uint32_t bk = key[0];
+        int bi = 0;
+#pragma unroll
+        for (int i = 1; i < VPL; ++i) {
+            const bool better = key[i] > bk;  // ascending e within the lane: ties keep the lower id
+            bk = better ? key[i] : bk;
+            bi = better ? i : bi;
         }
         const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
-        const int win = __reduce_min_sync(0xffffffffu, bk == kmax ? be : INT_MAX);
-        taken |= ((win & 31) == lane) ? (1u << (win >> 5)) : 0u;
-        const float v = row[win];
+        const int win = __reduce_min_sync(0xffffffffu, (bk == kmax && bk != 0u) ? lane + 32 * bi : INT_MAX);
+        const bool mine = (win & 31) == lane;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) key[i] = (mine && i == (win >> 5)) ? 0u : key[i];
+        // the winning key back to its value (route_key is invertible on finite values)
+        const float v = __uint_as_float((kmax & 0x80000000u) ? (kmax & 0x7FFFFFFFu) : ~kmax);
         vmax = (j == 0) ? v : vmax;
-        if (lane == 0) {
-            out_ids[j] = win;
-            out_w[j] = v;
-        }
-        __syncwarp();
+        if (lane == j) { id0 = win; v0 = v; }
+        if (lane + 32 == j) { id1 = win; v1 = v; }
     }
-    float sum = 0.f;
-    for (int j = lane; j < k; j += 32) {
-        const float ex = expf(out_w[j] - vmax);
-        out_w[j] = ex;
-        sum += ex;
-    }
+    const float ex0 = lane < k ? expf(v0 - vmax) : 0.f;
+    const float ex1 = lane + 32 < k ? expf(v1 - vmax) : 0.f;
+    float sum = ex0;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    __syncwarp();
+    if (k > 32) {
+        float s1 = ex1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+        sum += s1;
+    }
     const float inv_sum = 1.0f / sum;
-    for (int j = lane; j < k; j += 32) out_w[j] = out_w[j] * inv_sum;
+    if (lane < k) {
+        out_ids[lane] = id0;
+        out_w[lane] = ex0 * inv_sum;
+    }
+    if (lane + 32 < k) {
+        out_ids[lane + 32] = id1;
+        out_w[lane + 32] = ex1 * inv_sum;
+    }
     __syncwarp();
+}
+
+__device__ __forceinline__ void route_token(const float* row, int E, int k, int32_t* out_ids, float* out_w) {
+    const int nv = (E + 31) >> 5;
+    if (nv <= 1) route_token_regs<1>(row, E, k, out_ids, out_w);
+    else if (nv <= 2) route_token_regs<2>(row, E, k, out_ids, out_w);
+    else if (nv <= 4) route_token_regs<4>(row, E, k, out_ids, out_w);
+    else if (nv <= 8) route_token_regs<8>(row, E, k, out_ids, out_w);
+    else if (nv <= 16) route_token_regs<16>(row, E, k, out_ids, out_w);
+    else route_token_regs<32>(row, E, k, out_ids, out_w);
 }
 
 // -------------------------------------------------------- staged activations
@@ -327,21 +353,34 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     const int nslot = p.nslot;
 
     // ------------------------------------------------ phase 0: init, routing
+    // Scratch of phase 0 lives in the ring, which is idle until the producers
+    // start: the routed tokens' logits, then per-expert counts of the first and
+    // second 32 assignments and the touched-expert bitmask.
+    float* lgs = reinterpret_cast<float*>(sm);
+    int32_t* cnt_a = reinterpret_cast<int32_t*>(sm + p.off_cnt);
+    int32_t* cnt_b = cnt_a + E;
+    uint32_t* emask = reinterpret_cast<uint32_t*>(cnt_b + E);
+    int32_t* wpre = reinterpret_cast<int32_t*>(emask + 32);
     if (threadIdx.x == 0) tab.abort = 0;
-    if (warp == PRODUCER_WARP && lane == 0) {
-        for (int i = 0; i < NFULL; ++i) tc::mbar_init(full0 + 8u * i, FULL_ARRIVALS);
-        for (int i = 0; i < nslot; ++i) tc::mbar_init(empty0 + 8u * i, 2);
-        tc::fence_mbar_init();
-        tc::tma_prefetch_desc(&map13);
-        tc::tma_prefetch_desc(&map2);
+    if (warp == PRODUCER_WARP) {
+        for (int i = lane; i < NFULL; i += 32) tc::mbar_init(full0 + 8u * i, FULL_ARRIVALS);
+        for (int i = lane; i < nslot; i += 32) tc::mbar_init(empty0 + 8u * i, 2);
+        if (lane == 0) {
+            tc::fence_mbar_init();
+            tc::tma_prefetch_desc(&map13);
+            tc::tma_prefetch_desc(&map2);
+        }
+    } else if (warp == PRODUCER_WARP + 1) {
+        for (int i = lane; i < 2 * E; i += 32) cnt_a[i] = 0;
+        emask[lane] = 0;
     }
     if (warp < T) {
-        // this token's logits into the (still unused) ring, then top-k
-        float* lrow = reinterpret_cast<float*>(sm) + warp * E;
+        // this token's logits into shared memory, then top-k
+        float* lrow = lgs + warp * E;
         const float* src = p.logits + (size_t)warp * E;
         for (int e = lane; e < E; e += 32) lrow[e] = __ldg(src + e);
         __syncwarp();
-        route_token_smem(lrow, E, k, &tab.ids[warp * k], &tab.w[warp * k]);
+        route_token(lrow, E, k, &tab.ids[warp * k], &tab.w[warp * k]);
     } else if (warp < CW) {
         // activations -> fp16 in MMA order, plus C1/C2 per (token, group)
         const int nthr = (CW - T) * 32, tid = (warp - T) * 32 + lane;
@@ -371,50 +410,74 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     }
     __syncthreads();
     if (warp == 0) {
-        // stable counting sort of the R <= 64 assignments by expert (branch-free
-        // loop bodies keep the warp converged between the shuffles)
+        // stable counting sort of the R <= 64 assignments by expert: per-expert
+        // counts of the two halves, the touched-expert bitmask (ascending expert
+        // list by a warp scan), ranks inside an expert from __match_any_sync
+        const int a0 = lane, a1 = lane + 32;
+        const bool v0 = a0 < R, v1 = a1 < R;
+        const int e0 = v0 ? tab.ids[a0] : 0, e1 = v1 ? tab.ids[a1] : 0;
+        if (v0) {
+            atomicAdd(&cnt_a[e0], 1);
+            atomicOr(&emask[e0 >> 5], 1u << (e0 & 31));
+        }
+        if (v1) {
+            atomicAdd(&cnt_b[e1], 1);
+            atomicOr(&emask[e1 >> 5], 1u << (e1 & 31));
+        }
+        const uint32_t m0 = __match_any_sync(0xffffffffu, v0 ? e0 : -1 - lane);
+        const uint32_t m1 = __match_any_sync(0xffffffffu, v1 ? e1 : -1 - lane);
+        const uint32_t lt = (1u << lane) - 1u;
         __syncwarp();
-        const int e0 = lane < R ? tab.ids[lane] : INT_MAX;
-        const int e1 = lane + 32 < R ? tab.ids[lane + 32] : INT_MAX;
-        int r0 = 0, r1 = 0, n0 = 0, n1 = 0;
-        int f0 = lane < R, f1 = lane + 32 < R;
-        for (int a = 0; a < R; ++a) {
-            const int ea = __shfl_sync(0xffffffffu, a < 32 ? e0 : e1, a & 31);
-            const int eq0 = ea == e0, eq1 = ea == e1;
-            const int before0 = a < lane, before1 = a < lane + 32;
-            r0 += (ea < e0) | (eq0 & before0);
-            r1 += (ea < e1) | (eq1 & before1);
-            n0 += eq0;
-            n1 += eq1;
-            f0 &= !(eq0 & before0);
-            f1 &= !(eq1 & before1);
+        // ascending expert list: lane l owns bitmask word l
+        const uint32_t w = emask[lane];
+        int incl = __popc(w);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
-        int u0 = 0, u1 = 0;
-        for (int a = 0; a < R; ++a) {
-            const int ea = __shfl_sync(0xffffffffu, a < 32 ? e0 : e1, a & 31);
-            const int fa = __shfl_sync(0xffffffffu, a < 32 ? f0 : f1, a & 31);
-            u0 += fa & (ea < e0);
-            u1 += fa & (ea < e1);
-        }
-        if (lane < R) {
-            tab.pos[lane] = r0;
-            tab.ptok[r0] = lane / k;
-            if (f0) {
-                tab.uexp[u0] = e0;
-                tab.uoff[u0] = r0;
-                tab.ucnt[u0] = n0;
+        const int U = __shfl_sync(0xffffffffu, incl, 31);
+        int pre = incl - __popc(w);
+        wpre[lane] = pre;
+        for (uint32_t b = w; b; b &= b - 1) tab.uexp[pre++] = 32 * lane + (__ffs(b) - 1);
+        __syncwarp();
+        // expert counts and offsets in list order (U <= 64)
+        const int c0 = lane < U ? cnt_a[tab.uexp[lane]] + cnt_b[tab.uexp[lane]] : 0;
+        const int c1 = lane + 32 < U ? cnt_a[tab.uexp[lane + 32]] + cnt_b[tab.uexp[lane + 32]] : 0;
+        int s0 = c0, s1 = c1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y0 = __shfl_up_sync(0xffffffffu, s0, o);
+            const int y1 = __shfl_up_sync(0xffffffffu, s1, o);
+            if (lane >= o) {
+                s0 += y0;
+                s1 += y1;
             }
         }
-        if (lane + 32 < R) {
-            tab.pos[lane + 32] = r1;
-            tab.ptok[r1] = (lane + 32) / k;
-            if (f1) {
-                tab.uexp[u1] = e1;
-                tab.uoff[u1] = r1;
-                tab.ucnt[u1] = n1;
-            }
+        const int tot0 = __shfl_sync(0xffffffffu, s0, 31);
+        if (lane < U) {
+            tab.ucnt[lane] = c0;
+            tab.uoff[lane] = s0 - c0;
         }
-        const int U = __popc(__ballot_sync(0xffffffffu, f0)) + __popc(__ballot_sync(0xffffffffu, f1));
+        if (lane + 32 < U) {
+            tab.ucnt[lane + 32] = c1;
+            tab.uoff[lane + 32] = tot0 + s1 - c1;
+        }
+        __syncwarp();
+        // permuted position of each assignment
+        auto uidx = [&](int e) {
+            return wpre[e >> 5] + __popc(emask[e >> 5] & ((1u << (e & 31)) - 1u));
+        };
+        if (v0) {
+            const int pos = tab.uoff[uidx(e0)] + __popc(m0 & lt);
+            tab.pos[a0] = pos;
+            tab.ptok[pos] = a0 / k;
+        }
+        if (v1) {
+            const int pos = tab.uoff[uidx(e1)] + cnt_a[e1] + __popc(m1 & lt);
+            tab.pos[a1] = pos;
+            tab.ptok[pos] = a1 / k;
+        }
         if (lane == 0) tab.n_uniq = U;
     }
     __syncthreads();
@@ -425,25 +488,33 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     const int U = tab.n_uniq;
     const int nfb1 = f >> 3, nrb = d >> 4;
     const int N1 = U * nfb1, N2 = T * nrb;
-    const int a1 = (int)((long long)cta * N1 / G), b1 = (int)((long long)(cta + 1) * N1 / G);
-    const int a2 = (int)((long long)cta * N2 / G), b2 = (int)((long long)(cta + 1) * N2 / G);
+    // (32-bit products: N1 <= 64 * 2048 and N2 <= 8 * 1024, times G < 2^12)
+    const int a1 = cta * N1 / G, b1 = (cta + 1) * N1 / G;
+    const int a2 = cta * N2 / G, b2 = (cta + 1) * N2 / G;
     const int n1 = b1 - a1, n2u = b2 - a2, n2t = n2u * k;
     const int nch1 = ceil_div(Gd, CHUNK_GROUPS), nch2 = ceil_div(Gf, CHUNK_GROUPS);
 
     // ---------------------------------------------------------- producers
     if (warp >= PRODUCER_WARP) {
         const uint32_t pw = (uint32_t)(warp - PRODUCER_WARP);
-        uint32_t q = 0;
+        // chunk counter q = round * nslot + slot, kept incrementally (no division
+        // in the issue loop: a runtime divide costs tens of dependent instructions)
+        uint32_t q = 0, slot = 0, round = 0;
         bool ok = true;
+        auto advance = [&]() {
+            ++q;
+            if (++slot == (uint32_t)nslot) {
+                slot = 0;
+                ++round;
+            }
+        };
         auto issue = [&](const CUtensorMap* map, int row0, int row1, int chunk, const uint16_t* s_arr,
                          const uint16_t* z_arr, int Gk) {
-            if (q % NPROD != pw) {  // another producer warp's chunk
-                ++q;
+            if ((q & (NPROD - 1)) != pw) {  // another producer warp's chunk
+                advance();
                 return;
             }
-            const int slot = (int)(q % (uint32_t)nslot);
-            const uint32_t round = q / (uint32_t)nslot;
-            const uint32_t full = full0 + 8u * (q % NFULL), empty = empty0 + 8u * slot;
+            const uint32_t full = full0 + 8u * (q & (NFULL - 1)), empty = empty0 + 8u * slot;
             if (round > 0) {
                 // one lane waits and the warp follows its verdict; __syncwarp orders
                 // the consumers' last reads of the slot before any lane's new copies
@@ -471,20 +542,28 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             const uint32_t sdst = dst + SLOT_CODE + (uint32_t)(arr * SZ_ARRAY + r * 16);
             for (int i = 0; i < (gcv >> 1); ++i) cp_async4(sdst + 4u * i, src + 2 * i);
             tc::cp_async_mbar_arrive_noinc(full);
-            ++q;
+            advance();
         };
+        int u = a1 / nfb1, fb = a1 - u * nfb1;
         for (int tl = 0; tl < n1 && ok; ++tl) {
-            const int tau = a1 + tl, u = tau / nfb1, fb = tau - u * nfb1;
-            const int e = tab.uexp[u];
-            const int rg = e * 2 * f + 8 * fb;
+            const int rg = tab.uexp[u] * 2 * f + 8 * fb;
             for (int c = 0; c < nch1 && ok; ++c) issue(&map13, rg, rg + f, c, p.w13_s, p.w13_z, Gd);
+            if (++fb == nfb1) {
+                fb = 0;
+                ++u;
+            }
         }
+        int t = a2 / nrb, rb = a2 - t * nrb, j = 0;
         for (int i2 = 0; i2 < n2t && ok; ++i2) {
-            const int ups = a2 + i2 / k, j = i2 % k;
-            const int t = ups / nrb, rb = ups - t * nrb;
-            const int e = tab.ids[t * k + j];
-            const int rg = e * d + 16 * rb;
+            const int rg = tab.ids[t * k + j] * d + 16 * rb;
             for (int c = 0; c < nch2 && ok; ++c) issue(&map2, rg, rg + 8, c, p.w2_s, p.w2_z, Gf);
+            if (++j == k) {
+                j = 0;
+                if (++rb == nrb) {
+                    rb = 0;
+                    ++t;
+                }
+            }
         }
         // drain: the last use of every slot must have landed before the CTA exits
         // (each warp waits for its own chunks among the last nslot)
@@ -492,7 +571,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         const uint32_t first = issued > (uint32_t)nslot ? issued - (uint32_t)nslot : 0u;
         for (uint32_t qq = first; qq < issued; ++qq) {
             if (qq % NPROD != pw) continue;
-            const uint32_t full = full0 + 8u * (qq % NFULL);
+            const uint32_t full = full0 + 8u * (qq & (NFULL - 1));
             const uint32_t par = (qq / NFULL) & 1u;
             if (tc::mbar_try_wait(full, par)) continue;
             const uint64_t t0 = globaltimer_ns();
@@ -684,7 +763,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
 struct Layout {
     int nslot;
     size_t smem;
-    uint32_t off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab;
+    uint32_t off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab, off_cnt;
     int xb_stride, hs_stride;
 };
 
@@ -716,7 +795,9 @@ bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
     if (nslot < MIN_SLOTS) return false;
     const int nch_max = ceil_div(std::max(d, f) / 128, CHUNK_GROUPS);
     if (nslot + NPAIR * nch_max + 1 > NFULL) return false;
-    if ((size_t)T * E * 4 > (size_t)nslot * SLOT_BYTES) return false;  // logits staging
+    // phase-0 scratch in the ring: logits, two count arrays, bitmask, word prefixes
+    l.off_cnt = (uint32_t)align_up((size_t)T * E * 4, 16);
+    if (l.off_cnt + (size_t)8 * E + 256 > (size_t)nslot * SLOT_BYTES) return false;
     const uint32_t ring = (uint32_t)nslot * SLOT_BYTES;
     const uint32_t bars = (uint32_t)align_up((size_t)8 * (NFULL + nslot), 128);
     l.nslot = nslot;
@@ -781,6 +862,7 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     p.off_red = l.off_red;
     p.off_red2 = l.off_red2;
     p.off_tab = l.off_tab;
+    p.off_cnt = l.off_cnt;
     p.xb_stride = l.xb_stride;
     p.hs_stride = l.hs_stride;
 
