@@ -75,9 +75,9 @@ constexpr int SLOT_BYTES = SLOT_CODE + 1024;    // codes + scales + zeros, 1024-
 constexpr uint32_t FULL_ARRIVALS = 1 + 32;      // expect_tx arrival + 32 cp.async arrivals
 // "Full" barriers are indexed by chunk number modulo NFULL, not by ring slot:
 // the pairs consume different chunks, so a pair may wait for chunk q before
-// the chunk that last used q's ring slot has been consumed.  A pair runs at
-// most NPAIR tiles ahead of the chunks already issued, so with
-// NFULL >= nslot + NPAIR * (chunks per tile) + 1 the previous use of q's
+// the chunk that last used q's ring slot has been consumed.  A pair's next
+// chunk is at most NPAIR * (chunks per tile + 1) past its previous one, so with
+// NFULL >= nslot + NPAIR * (chunks per tile + 1) + 1 the previous use of q's
 // barrier (chunk q - NFULL) has always landed when q is waited on, and the
 // barrier's parity names q's phase unambiguously.
 constexpr int NFULL = 256;
@@ -544,26 +544,36 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             tc::cp_async_mbar_arrive_noinc(full);
             advance();
         };
-        int u = a1 / nfb1, fb = a1 - u * nfb1;
-        for (int tl = 0; tl < n1 && ok; ++tl) {
-            const int rg = tab.uexp[u] * 2 * f + 8 * fb;
-            for (int c = 0; c < nch1 && ok; ++c) issue(&map13, rg, rg + f, c, p.w13_s, p.w13_z, Gd);
-            if (++fb == nfb1) {
-                fb = 0;
-                ++u;
+        // Issue order: tiles in batches of NPAIR (one per pair); inside a batch,
+        // chunk c of every tile before chunk c + 1, so that every pair has data
+        // in the ring at once (the consumers' chunk numbering follows it).
+        // lane pp < NPAIR holds the first weight row of tile b0 + pp
+        for (int b0 = 0; b0 < n1 && ok; b0 += NPAIR) {
+            const int nb = min(NPAIR, n1 - b0);
+            int my_rg = 0;
+            if (lane < nb) {
+                const int tau = a1 + b0 + lane, u = tau / nfb1, fb = tau - u * nfb1;
+                my_rg = tab.uexp[u] * 2 * f + 8 * fb;
             }
-        }
-        int t = a2 / nrb, rb = a2 - t * nrb, j = 0;
-        for (int i2 = 0; i2 < n2t && ok; ++i2) {
-            const int rg = tab.ids[t * k + j] * d + 16 * rb;
-            for (int c = 0; c < nch2 && ok; ++c) issue(&map2, rg, rg + 8, c, p.w2_s, p.w2_z, Gf);
-            if (++j == k) {
-                j = 0;
-                if (++rb == nrb) {
-                    rb = 0;
-                    ++t;
+            for (int c = 0; c < nch1 && ok; ++c)
+                for (int pp = 0; pp < nb && ok; ++pp) {
+                    const int rg = __shfl_sync(0xffffffffu, my_rg, pp);
+                    issue(&map13, rg, rg + f, c, p.w13_s, p.w13_z, Gd);
                 }
+        }
+        for (int b0 = 0; b0 < n2t && ok; b0 += NPAIR) {
+            const int nb = min(NPAIR, n2t - b0);
+            int my_rg = 0;
+            if (lane < nb) {
+                const int i2 = b0 + lane, ul = i2 / k, j = i2 - ul * k;
+                const int ups = a2 + ul, t = ups / nrb, rb = ups - t * nrb;
+                my_rg = tab.ids[t * k + j] * d + 16 * rb;
             }
+            for (int c = 0; c < nch2 && ok; ++c)
+                for (int pp = 0; pp < nb && ok; ++pp) {
+                    const int rg = __shfl_sync(0xffffffffu, my_rg, pp);
+                    issue(&map2, rg, rg + 8, c, p.w2_s, p.w2_z, Gf);
+                }
         }
         // drain: the last use of every slot must have landed before the CTA exits
         // (each warp waits for its own chunks among the last nslot)
@@ -616,8 +626,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         const uint32_t brow_a = xb + (uint32_t)(brow * p.xb_stride);
         const uint32_t c0_a = cxa + (uint32_t)(cr0 * Gd * 8), c1_a = cxa + (uint32_t)(cr1 * Gd * 8);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int b0 = tl - pair, nb = min(NPAIR, n1 - b0);
         for (int c = 0; c < nch1; ++c) {
-            const uint32_t q = (uint32_t)(tl * nch1 + c);
+            const uint32_t q = (uint32_t)(b0 * nch1 + c * nb + pair);  // interleaved issue order
             const int slot = (int)(q % (uint32_t)nslot);
             const bool ready = tc::mbar_wait(full0 + 8u * (q % NFULL), (q / NFULL) & 1u, abort_flag, p.err);
             if (ready) {
@@ -725,8 +736,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             const int cr0 = t4 == 0 ? lr : zrow;
             const uint32_t brow_a = hs + (uint32_t)(brow * p.hs_stride);
             const uint32_t c0_a = cha + (uint32_t)(cr0 * Gf * 8), c1_a = cha + (uint32_t)(zrow * Gf * 8);
+            const int b0 = i2 - pair, nb = min(NPAIR, n2t - b0);
             for (int c = 0; c < nch2; ++c) {
-                const uint32_t q = qbase + (uint32_t)(i2 * nch2 + c);
+                const uint32_t q = qbase + (uint32_t)(b0 * nch2 + c * nb + pair);  // interleaved issue order
                 const int slot = (int)(q % (uint32_t)nslot);
                 const bool ready =
                     tc::mbar_wait(full0 + 8u * (q % NFULL), (q / NFULL) & 1u, abort_flag, p.err);
@@ -780,11 +792,15 @@ bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
         fixed = align_up(fixed + bytes, 128);
         return (uint32_t)o;
     };
-    // offsets relative to the end of the ring and its barriers (rebased below)
-    const uint32_t o_xb = take((size_t)(T + 1) * l.xb_stride);
-    const uint32_t o_cx = take((size_t)(T + 1) * (d / 128) * 8);
-    const uint32_t o_hs = take((size_t)(2 * k + 1) * l.hs_stride);
-    const uint32_t o_ch = take((size_t)(2 * k + 1) * (f / 128) * 8);
+    // offsets relative to the end of the ring and its barriers (rebased below).
+    // The staged activations (+ C1/C2) are read in phase 1 only and the staged
+    // h rows (+ C1/C2) are written after the grid barrier: one shared region.
+    const size_t sx = align_up((size_t)(T + 1) * l.xb_stride, 128) + (size_t)(T + 1) * (d / 128) * 8;
+    const size_t sh = align_up((size_t)(2 * k + 1) * l.hs_stride, 128) + (size_t)(2 * k + 1) * (f / 128) * 8;
+    const uint32_t o_xb = take(std::max(sx, sh));
+    const uint32_t o_cx = o_xb + (uint32_t)align_up((size_t)(T + 1) * l.xb_stride, 128);
+    const uint32_t o_hs = o_xb;
+    const uint32_t o_ch = o_xb + (uint32_t)align_up((size_t)(2 * k + 1) * l.hs_stride, 128);
     const uint32_t o_red = take((size_t)NPAIR * 2 * 32 * 4 * 4);
     const uint32_t o_red2 = take((size_t)n2u_max * NPAIR * 16 * 4);
     const uint32_t o_tab = take(sizeof(Tab));
@@ -794,7 +810,7 @@ bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
     nslot = std::min(nslot, 32);
     if (nslot < MIN_SLOTS) return false;
     const int nch_max = ceil_div(std::max(d, f) / 128, CHUNK_GROUPS);
-    if (nslot + NPAIR * nch_max + 1 > NFULL) return false;
+    if (nslot + NPAIR * (nch_max + 1) + 1 > NFULL) return false;
     // phase-0 scratch in the ring: logits, two count arrays, bitmask, word prefixes
     l.off_cnt = (uint32_t)align_up((size_t)T * E * 4, 16);
     if (l.off_cnt + (size_t)8 * E + 256 > (size_t)nslot * SLOT_BYTES) return false;
