@@ -43,9 +43,10 @@
 // lane 0 issues 3D TMA boxes of the packed codes (16 rows x 4 lines of 128 B =
 // 2 groups each, 128-byte swizzle) into a ring of slots and all lanes copy
 // the matching fp16 scales and zeros with 4-byte cp.async, tracked by the
-// chunk's full mbarrier.  Warps 0..15 form 8
-// pairs; a tile belongs to one pair and each warp of the pair takes half of
-// every chunk's groups; the two halves are added through shared memory.
+// chunk's full mbarrier.  Warps 0..15 form 8 pairs; a tile belongs to one pair
+// and each warp of the pair takes half of every chunk's groups (the slot is
+// released after the warp's last copy from it); the two halves are added
+// through shared memory.
 // Every wait is bounded (2 s), after which the kernel records a timeout in the
 // workspace error word, raises the CTA's abort flag and winds down.
 #include <cfloat>
@@ -59,7 +60,7 @@ namespace {
 
 using tc::WAIT_LIMIT_NS;
 
-constexpr int CW = 16;                          // consumer warps
+constexpr int CW = 16;                          // consumer warps (8 pairs)
 constexpr int NPAIR = CW / 2;
 constexpr int PRODUCER_WARP = CW;               // first producer warp
 constexpr int NPROD = 4;                        // producer warps: chunk q is issued by warp q % NPROD
@@ -290,23 +291,38 @@ __device__ __forceinline__ float2 halfwarp_sum(float2 v) {
     return v;
 }
 
-// One group (128 codes) of one 16-row tile for this warp: 8 MMAs and the
-// group epilogue into acc.  sa: slot address; gl: group inside the chunk;
-// bg: staged B row address of this lane's column at the group;
-// c0, c1: C1/C2 addresses of columns 2t and 2t+1 at the group; wscale: factor
-// applied to the scales (routing weight in phase 2).
-__device__ __forceinline__ void tile_group(float (&acc)[4], uint32_t sa, int gl, int g, int t, uint32_t bg,
-                                           uint32_t c0, uint32_t c1, float wscale) {
+// One group (128 codes) of one 16-row tile, as this warp takes it from a ring
+// slot: the packed words of rows g and g + 8 (words 4t..4t+3 of the group)
+// and the two rows' scales and zeros.  sa: slot address; gl: group inside the
+// chunk.  Loading all of a chunk's groups first lets the warp give the slot
+// back before it computes.
+struct GroupA {
+    uint4 wa, wb;
+    float s0, z0, s1, z1;
+};
+__device__ __forceinline__ void load_group(GroupA& ga, uint32_t sa, int gl, int g, int t) {
     const int ell = gl >> 1;
     const uint32_t phys = (uint32_t)((((gl & 1) << 2) | t) ^ (((g & 1) << 2) | ell));
     const uint32_t aoff = (uint32_t)(g * 512 + ell * 128) + (phys << 4);
-    const uint4 wa = lds128(sa + aoff);              // row g: words 4t..4t+3 of the group
-    const uint4 wb = lds128(sa + BOX_BYTES + aoff);  // row g + 8
+    ga.wa = lds128(sa + aoff);              // row g
+    ga.wb = lds128(sa + BOX_BYTES + aoff);  // row g + 8
+    const uint32_t szb = sa + SLOT_CODE + (uint32_t)(gl * 2);
+    ga.s0 = lds_half(szb + g * 16);
+    ga.z0 = lds_half(szb + SZ_ARRAY + g * 16);
+    ga.s1 = lds_half(szb + (8 + g) * 16);
+    ga.z1 = lds_half(szb + SZ_ARRAY + (8 + g) * 16);
+}
+
+// The group's 8 MMAs and its epilogue into acc.  bg: staged B row address of
+// this lane's column at the group; c0, c1: C1/C2 addresses of columns 2t and
+// 2t + 1 at the group; wscale: factor on the scales (routing weight in phase 2).
+__device__ __forceinline__ void compute_group(float (&acc)[4], const GroupA& ga, int t, uint32_t bg, uint32_t c0,
+                                              uint32_t c1, float wscale) {
     uint4 b[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) b[i] = lds128(bg + ((uint32_t)stage_word(4 * t + i) << 4));
-    const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
-    const uint32_t Bw[4] = {wb.x, wb.y, wb.z, wb.w};
+    const uint32_t A[4] = {ga.wa.x, ga.wa.y, ga.wa.z, ga.wa.w};
+    const uint32_t Bw[4] = {ga.wb.x, ga.wb.y, ga.wb.z, ga.wb.w};
     float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -323,16 +339,39 @@ __device__ __forceinline__ void tile_group(float (&acc)[4], uint32_t sa, int gl,
         const uint32_t e3 = lop_mask_or(ys, 0x00F000F0u, 0x54005400u);
         mma16816(db, e0, e1, e2, e3, b[i].z, b[i].w);
     }
-    const uint32_t szb = sa + SLOT_CODE + (uint32_t)(gl * 2);
-    const float s0 = lds_half(szb + g * 16) * wscale;
-    const float z0 = lds_half(szb + SZ_ARRAY + g * 16);
-    const float s1 = lds_half(szb + (8 + g) * 16) * wscale;
-    const float z1 = lds_half(szb + SZ_ARRAY + (8 + g) * 16);
+    const float s0 = ga.s0 * wscale, s1 = ga.s1 * wscale;
     const float2 ca = lds_f2(c0), cb = lds_f2(c1);
-    acc[0] = fmaf(s0, (da[0] + db[0]) - fmaf(z0, ca.y, ca.x), acc[0]);
-    acc[1] = fmaf(s0, (da[1] + db[1]) - fmaf(z0, cb.y, cb.x), acc[1]);
-    acc[2] = fmaf(s1, (da[2] + db[2]) - fmaf(z1, ca.y, ca.x), acc[2]);
-    acc[3] = fmaf(s1, (da[3] + db[3]) - fmaf(z1, cb.y, cb.x), acc[3]);
+    acc[0] = fmaf(s0, (da[0] + db[0]) - fmaf(ga.z0, ca.y, ca.x), acc[0]);
+    acc[1] = fmaf(s0, (da[1] + db[1]) - fmaf(ga.z0, cb.y, cb.x), acc[1]);
+    acc[2] = fmaf(s1, (da[2] + db[2]) - fmaf(ga.z1, ca.y, ca.x), acc[2]);
+    acc[3] = fmaf(s1, (da[3] + db[3]) - fmaf(ga.z1, cb.y, cb.x), acc[3]);
+}
+
+// A chunk for this warp: wait for it, then for each of this warp's groups
+// (half of the chunk's gcv groups) copy the group into registers and compute
+// it; the slot is given back right after the last group's copy, before its
+// math.
+__device__ __forceinline__ void consume_chunk(float (&acc)[4], uint32_t full, uint32_t empty, uint32_t parity,
+                                              uint32_t sa, int gcv, int half, int g, int t, int gi0, uint32_t brow_a,
+                                              uint32_t c0_a, uint32_t c1_a, float wscale, volatile int* abort_flag,
+                                              uint32_t* err) {
+    const bool ready = tc::mbar_wait(full, parity, abort_flag, err);
+    const int ng = gcv >> 1, gb = half * ng;
+    if (!ready) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty);
+        return;
+    }
+    for (int i = 0; i < ng; ++i) {
+        GroupA ga;
+        load_group(ga, sa, gb + i, g, t);
+        if (i == ng - 1) {
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty);
+        }
+        const int gi = gi0 + gb + i;
+        compute_group(acc, ga, t, brow_a + 256u * gi, c0_a + 8u * gi, c1_a + 8u * gi, wscale);
+    }
 }
 
 // ------------------------------------------------------------------ kernel
@@ -630,18 +669,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         for (int c = 0; c < nch1; ++c) {
             const uint32_t q = (uint32_t)(b0 * nch1 + c * nb + pair);  // interleaved issue order
             const int slot = (int)(q % (uint32_t)nslot);
-            const bool ready = tc::mbar_wait(full0 + 8u * (q % NFULL), (q / NFULL) & 1u, abort_flag, p.err);
-            if (ready) {
-                const int gcv = min(CHUNK_GROUPS, Gd - c * CHUNK_GROUPS);
-                const int gb = half * (gcv >> 1), ge = gb + (gcv >> 1);
-                const uint32_t sa = sbase + (uint32_t)slot * SLOT_BYTES;
-                for (int gl = gb; gl < ge; ++gl) {
-                    const int gi = c * CHUNK_GROUPS + gl;
-                    tile_group(acc, sa, gl, g, t4, brow_a + 256u * gi, c0_a + 8u * gi, c1_a + 8u * gi, 1.0f);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(empty0 + 8u * slot);
+            consume_chunk(acc, full0 + 8u * (q % NFULL), empty0 + 8u * slot, (q / NFULL) & 1u,
+                          sbase + (uint32_t)slot * SLOT_BYTES, min(CHUNK_GROUPS, Gd - c * CHUNK_GROUPS), half, g,
+                          t4, c * CHUNK_GROUPS, brow_a, c0_a, c1_a, 1.0f, abort_flag, p.err);
         }
         pair_reduce(acc);
         if (half == 0 && !*abort_flag) {
@@ -740,19 +770,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             for (int c = 0; c < nch2; ++c) {
                 const uint32_t q = qbase + (uint32_t)(b0 * nch2 + c * nb + pair);  // interleaved issue order
                 const int slot = (int)(q % (uint32_t)nslot);
-                const bool ready =
-                    tc::mbar_wait(full0 + 8u * (q % NFULL), (q / NFULL) & 1u, abort_flag, p.err);
-                if (ready) {
-                    const int gcv = min(CHUNK_GROUPS, Gf - c * CHUNK_GROUPS);
-                    const int gb = half * (gcv >> 1), ge = gb + (gcv >> 1);
-                    const uint32_t sa = sbase + (uint32_t)slot * SLOT_BYTES;
-                    for (int gl = gb; gl < ge; ++gl) {
-                        const int gi = c * CHUNK_GROUPS + gl;
-                        tile_group(acc, sa, gl, g, t4, brow_a + 256u * gi, c0_a + 8u * gi, c1_a + 8u * gi, wj);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(empty0 + 8u * slot);
+                consume_chunk(acc, full0 + 8u * (q % NFULL), empty0 + 8u * slot, (q / NFULL) & 1u,
+                              sbase + (uint32_t)slot * SLOT_BYTES, min(CHUNK_GROUPS, Gf - c * CHUNK_GROUPS), half, g,
+                              t4, c * CHUNK_GROUPS, brow_a, c0_a, c1_a, wj, abort_flag, p.err);
             }
         }
         if (cur >= 0) flush(cur);
