@@ -210,6 +210,12 @@ moe_status_t moe_combine(const void* y_perm_bf16, const int32_t* inv, const floa
 
 /*
  * The whole layer: stages 1-4 on one stream, nothing allocated, no host sync.
+ * With T <= 8 and T*k <= 64 the layer runs as ONE kernel (routing repeated in
+ * every CTA, gate_up, one grid barrier, down with the combine fused; one CTA
+ * per SM, cooperative launch).  Its intermediate precision: activations and h
+ * in fp16 (|x|, |h| < 65504, else MOE_ERR_F16_RANGE), products of the exact
+ * int4 codes with fp32 accumulation, zero and scale applied per group of 128
+ * in fp32.  MOE_W4_DECODE_KERNEL=split runs the stage chain instead.
  *
  *   x        device bf16 [T][d_model]
  *   logits   device fp32 [T][E]
@@ -226,7 +232,9 @@ size_t moe_layer_workspace_size(const moe_w4_layer* L, int32_t T, int32_t k);
 /*
  * Reads and clears the device error word kept at the start of a workspace
  * used by moe_permute, moe_expert_ffn_w4a16 or moe_layer_forward.  Waits for
- * `stream` to finish.  Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_RANGE
+ * `stream` to finish.  When it reports an error it clears the whole 256-byte
+ * header, which also holds the grid-barrier counter of the one-kernel decode
+ * layer (a call that gave up can leave that counter inconsistent).  Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_RANGE
  * or MOE_ERR_F16_RANGE, in that order of precedence (or MOE_ERR_CUDA if the
  * copy fails).
  */
