@@ -47,9 +47,16 @@ struct StageMarks {
         }
     }
     void mark(int i) {
-        // external record: inside a stream capture this becomes an event-record
-        // node of the graph, so replays time the stages too
-        if (ev) cudaEventRecordWithFlags(ev[i], s, cudaEventRecordExternal);
+        if (!ev) return;
+        // inside a stream capture an external record becomes an event-record
+        // node of the graph, so replays time the stages too; outside a capture
+        // a plain record.  A failed record must not surface as a launch error.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaStreamIsCapturing(s, &cs);
+        const cudaError_t e = (cs == cudaStreamCaptureStatusActive)
+                                  ? cudaEventRecordWithFlags(ev[i], s, cudaEventRecordExternal)
+                                  : cudaEventRecord(ev[i], s);
+        if (e != cudaSuccess) (void)cudaGetLastError();
     }
 };
 

@@ -128,7 +128,9 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+// SiLU(g) = g / (1 + e^-g) with the fast exponential and division (a few ulp;
+// g -> -inf gives -0 since the quotient by an infinite denominator is 0).
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;

@@ -337,6 +337,9 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 uint32_t v[32];
                 tc::tmem_ld_32x32b_x32(tmem_base + buf * 256 + cb * 32 + ((uint32_t)(32 * q) << 16), v);
                 tc::tmem_ld_wait();
+                // out-of-range fp16 values are collected per column block and
+                // reported once (a branch per element costs more than the math)
+                uint32_t bad = 0;
                 if (GATEUP) {
                     const bool lo_half = lane < 16;
                     const int feat = fb * 64 + 16 * q + (lane & 15);
@@ -347,31 +350,40 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                         const float g = __uint_as_float(lo_half ? v[j] : recv);
                         const float u = __uint_as_float(lo_half ? recv : v[16 + j]);
                         const int col = cb * 32 + (lo_half ? j : 16 + j);
-                        if (col < nrows) {
-                            const uint16_t hb = float_to_f16_bits(silu(g) * u);
-                            if ((hb & 0x7C00u) == 0x7C00u) set_error(p.err, ERRBIT_F16_RANGE);
-                            p.out[(size_t)(row0 + col) * p.out_ld + feat] = hb;
-                        }
+                        const uint16_t hb = float_to_f16_bits(silu(g) * u);
+                        const bool valid = col < nrows;  // later columns hold the next expert's rows
+                        bad |= valid & ((hb & 0x7C00u) == 0x7C00u);
+                        if (valid) p.out[(size_t)(row0 + col) * p.out_ld + feat] = hb;
                     }
                 } else {
                     const int feat = fb * BM + 32 * q + lane;
+                    uint16_t* outp = p.out + (size_t)(row0 + cb * 32) * p.out_ld + feat;
+                    const int ncol = min(32, nrows - cb * 32);
+                    if (p.row_w) {
+                        const float* rw = p.row_w + row0 + cb * 32;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = cb * 32 + j;
-                        if (col < nrows) {
-                            float y = __uint_as_float(v[j]);
-                            if (p.row_w) y *= p.row_w[row0 + col];
-                            uint16_t yb;
-                            if (p.out_f16) {
-                                yb = float_to_f16_bits(y);
-                                if ((yb & 0x7C00u) == 0x7C00u) set_error(p.err, ERRBIT_F16_RANGE);
-                            } else {
-                                yb = float_to_bf16_bits(y);
+                        for (int j = 0; j < 32; ++j)
+                            if (j < ncol) {
+                                const float y = __uint_as_float(v[j]) * rw[j];
+                                const uint16_t yb = p.out_f16 ? float_to_f16_bits(y) : float_to_bf16_bits(y);
+                                bad |= p.out_f16 && ((yb & 0x7C00u) == 0x7C00u);
+                                outp[(size_t)j * p.out_ld] = yb;
                             }
-                            p.out[(size_t)(row0 + col) * p.out_ld + feat] = yb;
-                        }
+                    } else if (p.out_f16) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < ncol) {
+                                const uint16_t yb = float_to_f16_bits(__uint_as_float(v[j]));
+                                bad |= ((yb & 0x7C00u) == 0x7C00u);
+                                outp[(size_t)j * p.out_ld] = yb;
+                            }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < ncol) outp[(size_t)j * p.out_ld] = float_to_bf16_bits(__uint_as_float(v[j]));
                     }
                 }
+                if (bad) set_error(p.err, ERRBIT_F16_RANGE);
             }
             tc::tc_fence_before();
             __syncwarp();
