@@ -38,12 +38,14 @@
 //     C1 = 1024 * sum(x over even k) + 64 * sum(x over odd k),   C2 = sum(x),
 // with C1 and C2 computed once per (token, group) from the same fp16 values.
 //
-// Pipeline.  Warps 16..19 are producers (chunk q belongs to warp 16 + q % 4,
-// since issuing one chunk keeps a warp busy for about a thousand cycles):
-// lane 0 issues 3D TMA boxes of the packed codes (16 rows x 4 lines of 128 B =
-// 2 groups each, 128-byte swizzle) into a ring of slots and all lanes copy
-// the matching fp16 scales and zeros with 4-byte cp.async, tracked by the
-// chunk's full mbarrier.  Warps 0..15 form 8 pairs; a tile belongs to one pair
+// Pipeline.  Warps 16..19 are producers.  Lane 0 of warp 16 takes every chunk
+// in order: it waits until the chunk's ring slot is empty, issues 3D TMA boxes
+// of the packed codes (16 rows x 4 lines of 128 B = 2 groups each, 128-byte
+// swizzle) and marks the slot issued.  Warps 17..19 (chunk q to warp
+// 17 + q % 3, since copying a chunk's scales keeps a warp busy for several
+// hundred cycles) wait for that mark and copy the matching fp16 scales and
+// zeros with 4-byte cp.async; TMA bytes and copies complete the chunk's full
+// mbarrier.  Warps 0..15 form 8 pairs; a tile belongs to one pair
 // and each warp of the pair takes half of every chunk's groups (the slot is
 // released after the warp's last copy from it); the two halves are added
 // through shared memory.
@@ -62,32 +64,33 @@ using tc::WAIT_LIMIT_NS;
 
 constexpr int CW = 16;                          // consumer warps (8 pairs)
 constexpr int NPAIR = CW / 2;
+constexpr int NQ = 4;                           // pipelines: producer warp 16 + i feeds pairs 2i and 2i + 1
 constexpr int PRODUCER_WARP = CW;               // first producer warp
-constexpr int NPROD = 4;                        // producer warps: chunk q is issued by warp q % NPROD
-static_assert((NPROD & (NPROD - 1)) == 0, "NPROD must be a power of two");
-constexpr int NTHREADS = 32 * (CW + NPROD);
+constexpr int NTHREADS = 32 * (CW + NQ);
 constexpr int CONSUMER_THREADS = 32 * CW;
 constexpr int LINES = 4;                        // 128-byte lines (2 groups each) per chunk row
 constexpr int CHUNK_GROUPS = 2 * LINES;         // groups of 128 codes per chunk
 constexpr int BOX_BYTES = 8 * LINES * 128;      // one TMA box: 8 rows x 4 lines
-constexpr int SLOT_CODE = 2 * BOX_BYTES;        // 16 rows of codes
+constexpr int SLOT_CODE = 2 * BOX_BYTES;        // 16 rows of codes (a multiple of the 1024-byte swizzle atom)
 constexpr int SZ_ARRAY = 16 * CHUNK_GROUPS * 2; // fp16 [16 rows][8 groups]
-constexpr int SLOT_BYTES = SLOT_CODE + 1024;    // codes + scales + zeros, 1024-byte aligned
-constexpr uint32_t FULL_ARRIVALS = 1 + 32;      // expect_tx arrival + 32 cp.async arrivals
-// "Full" barriers are indexed by chunk number modulo NFULL, not by ring slot:
-// the pairs consume different chunks, so a pair may wait for chunk q before
-// the chunk that last used q's ring slot has been consumed.  A pair's next
-// chunk is at most NPAIR * (chunks per tile + 1) past its previous one, so with
-// NFULL >= nslot + NPAIR * (chunks per tile + 1) + 1 the previous use of q's
-// barrier (chunk q - NFULL) has always landed when q is waited on, and the
-// barrier's parity names q's phase unambiguously.
-constexpr int NFULL = 256;
-static_assert((NFULL & (NFULL - 1)) == 0, "NFULL must be a power of two");
+constexpr int SLOT_SZ = 2 * SZ_ARRAY;           // scales, then zeros
+constexpr uint32_t FULL_ARRIVALS = 1 + 32;      // expect_tx arrival + one cp.async arrival per producer lane
+// Each pipeline numbers its chunks in issue order and indexes its "full"
+// barriers by chunk number modulo NFQ (not by ring slot: the pipeline's two
+// pairs consume different chunks, so a pair may wait for chunk q before the
+// chunk that last used q's slot has been consumed).  The pipeline's producer
+// issues in order and issues chunk x only once chunk x - ns4 (ns4: its slots)
+// has been consumed, so every chunk up to x - ns4 has landed by then; a pair's
+// next chunk is at most 2 past its previous one, so with NFQ >= ns4 + 3 the
+// previous use of q's barrier (chunk q - NFQ) has landed when q is waited on
+// and the barrier's parity names q's phase unambiguously.
+constexpr int NFQ = 64;
+static_assert((NFQ & (NFQ - 1)) == 0, "NFQ must be a power of two");
 constexpr int MAX_T = 8;
 constexpr int MAX_R = 64;
 constexpr int ROW_PAD = 64;                     // bytes after each staged activation row
 constexpr size_t SMEM_LIMIT = 232448;
-constexpr int MIN_SLOTS = 6;
+constexpr int MAX_SLOTS = 32;
 
 struct Tab {
     int32_t ids[MAX_R];    // routing, slot a = t*k + j
@@ -112,8 +115,8 @@ struct Params {
     uint32_t* err;
     unsigned long long* bar_count;  // grid-barrier arrivals (only grows)
     int T, k, E, d, f;
-    int nslot;
-    uint32_t off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab;
+    int nslot;                 // a multiple of NQ: pipeline i owns slots [i * nslot / NQ, (i + 1) * nslot / NQ)
+    uint32_t off_sz, off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab;
     uint32_t off_cnt;          // phase-0 counters inside the ring, after the logits
     int xb_stride, hs_stride;  // bytes per staged row
 };
@@ -129,10 +132,20 @@ __device__ __forceinline__ float2 lds_f2(uint32_t a) {
     asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
     return v;
 }
-__device__ __forceinline__ float lds_half(uint32_t a) {
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
     uint16_t h;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
-    return __half2float(__ushort_as_half(h));
+    return h;
+}
+// 16-byte shared load done only by lanes with `active` set (others get zeros):
+// lanes that skip it issue no shared-memory wavefronts.
+__device__ __forceinline__ uint4 lds128_if(uint32_t a, uint32_t active) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %5, 0;\n\t"
+        "@p ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w) : "r"(a), "r"(active));
+    return v;
 }
 __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" :: "r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
@@ -291,38 +304,28 @@ __device__ __forceinline__ float2 halfwarp_sum(float2 v) {
     return v;
 }
 
-// One group (128 codes) of one 16-row tile, as this warp takes it from a ring
-// slot: the packed words of rows g and g + 8 (words 4t..4t+3 of the group)
-// and the two rows' scales and zeros.  sa: slot address; gl: group inside the
-// chunk.  Loading all of a chunk's groups first lets the warp give the slot
-// back before it computes.
-struct GroupA {
-    uint4 wa, wb;
-    float s0, z0, s1, z1;
-};
-__device__ __forceinline__ void load_group(GroupA& ga, uint32_t sa, int gl, int g, int t) {
+// Offset of this lane's 16 bytes of group gl of row g inside a slot's codes
+// (row g + 8 is the same offset in the second box): the TMA box's 128-byte
+// swizzle XORs the 16-byte unit index with the row's index inside the
+// 1024-byte swizzle atom.
+__device__ __forceinline__ uint32_t a_offset(int gl, int g, int t) {
     const int ell = gl >> 1;
     const uint32_t phys = (uint32_t)((((gl & 1) << 2) | t) ^ (((g & 1) << 2) | ell));
-    const uint32_t aoff = (uint32_t)(g * 512 + ell * 128) + (phys << 4);
-    ga.wa = lds128(sa + aoff);              // row g
-    ga.wb = lds128(sa + BOX_BYTES + aoff);  // row g + 8
-    const uint32_t szb = sa + SLOT_CODE + (uint32_t)(gl * 2);
-    ga.s0 = lds_half(szb + g * 16);
-    ga.z0 = lds_half(szb + SZ_ARRAY + g * 16);
-    ga.s1 = lds_half(szb + (8 + g) * 16);
-    ga.z1 = lds_half(szb + SZ_ARRAY + (8 + g) * 16);
+    return (uint32_t)(g * 512 + ell * 128) + (phys << 4);
 }
 
-// The group's 8 MMAs and its epilogue into acc.  bg: staged B row address of
-// this lane's column at the group; c0, c1: C1/C2 addresses of columns 2t and
-// 2t + 1 at the group; wscale: factor on the scales (routing weight in phase 2).
-__device__ __forceinline__ void compute_group(float (&acc)[4], const GroupA& ga, int t, uint32_t bg, uint32_t c0,
-                                              uint32_t c1, float wscale) {
+// The group's 8 MMAs and its epilogue into acc.  wa, wb: this lane's packed
+// words of rows g and g + 8; s0, z0, s1, z1: the two rows' scale and zero;
+// bg: staged B row address of this lane's column at the group (loaded only
+// where bact is set: B columns without a token are zero); c0, c1: C1/C2
+// addresses of columns 2t and 2t + 1 at the group.
+__device__ __forceinline__ void compute_group(float (&acc)[4], uint4 wa, uint4 wb, float s0, float z0, float s1,
+                                              float z1, int t, uint32_t bg, uint32_t bact, uint32_t c0, uint32_t c1) {
     uint4 b[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) b[i] = lds128(bg + ((uint32_t)stage_word(4 * t + i) << 4));
-    const uint32_t A[4] = {ga.wa.x, ga.wa.y, ga.wa.z, ga.wa.w};
-    const uint32_t Bw[4] = {ga.wb.x, ga.wb.y, ga.wb.z, ga.wb.w};
+    for (int i = 0; i < 4; ++i) b[i] = lds128_if(bg + ((uint32_t)stage_word(4 * t + i) << 4), bact);
+    const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t Bw[4] = {wb.x, wb.y, wb.z, wb.w};
     float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -339,38 +342,86 @@ __device__ __forceinline__ void compute_group(float (&acc)[4], const GroupA& ga,
         const uint32_t e3 = lop_mask_or(ys, 0x00F000F0u, 0x54005400u);
         mma16816(db, e0, e1, e2, e3, b[i].z, b[i].w);
     }
-    const float s0 = ga.s0 * wscale, s1 = ga.s1 * wscale;
     const float2 ca = lds_f2(c0), cb = lds_f2(c1);
-    acc[0] = fmaf(s0, (da[0] + db[0]) - fmaf(ga.z0, ca.y, ca.x), acc[0]);
-    acc[1] = fmaf(s0, (da[1] + db[1]) - fmaf(ga.z0, cb.y, cb.x), acc[1]);
-    acc[2] = fmaf(s1, (da[2] + db[2]) - fmaf(ga.z1, ca.y, ca.x), acc[2]);
-    acc[3] = fmaf(s1, (da[3] + db[3]) - fmaf(ga.z1, cb.y, cb.x), acc[3]);
+    acc[0] = fmaf(s0, (da[0] + db[0]) - fmaf(z0, ca.y, ca.x), acc[0]);
+    acc[1] = fmaf(s0, (da[1] + db[1]) - fmaf(z0, cb.y, cb.x), acc[1]);
+    acc[2] = fmaf(s1, (da[2] + db[2]) - fmaf(z1, ca.y, ca.x), acc[2]);
+    acc[3] = fmaf(s1, (da[3] + db[3]) - fmaf(z1, cb.y, cb.x), acc[3]);
 }
 
-// A chunk for this warp: wait for it, then for each of this warp's groups
-// (half of the chunk's gcv groups) copy the group into registers and compute
-// it; the slot is given back right after the last group's copy, before its
-// math.
+__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFFu))); }
+__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
+
+// This warp's NG groups (gb .. gb + NG - 1 of the chunk whose codes are at sa
+// and whose scales and zeros are at szs): all of
+// their codes, scales and zeros are copied into registers first and the slot
+// is given back before any math, so a slot is held only for the copy.
+template <int NG>
+__device__ __forceinline__ void consume_groups(float (&acc)[4], uint32_t sa, uint32_t szs, uint32_t empty, int gb,
+                                               int g, int t, int gi0, uint32_t brow_a, uint32_t bact, uint32_t c0_a,
+                                               uint32_t c1_a, float wscale) {
+    uint4 wa[NG], wb[NG];
+#pragma unroll
+    for (int i = 0; i < NG; ++i) {
+        const uint32_t aoff = a_offset(gb + i, g, t);
+        wa[i] = lds128(sa + aoff);
+        wb[i] = lds128(sa + BOX_BYTES + aoff);
+    }
+    // scales and zeros kept as fp16 pairs until use: sz[0..3] = s0, z0, s1, z1
+    // (rows g and g + 8), word w holds groups 2w and 2w + 1 of this warp's NG
+    constexpr int NW = (NG + 1) / 2;
+    uint32_t sz[4][NW];
+    const uint32_t szb = szs + (uint32_t)(gb * 2 + g * 16);
+    const uint32_t sza[4] = {szb, szb + SZ_ARRAY, szb + 128, szb + SZ_ARRAY + 128};
+    if constexpr (NG == 4) {
+        // four groups' values of one row are 8 aligned bytes (gb is 0 or 4)
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float2 v = lds_f2(sza[a]);
+            sz[a][0] = __float_as_uint(v.x);
+            sz[a][1] = __float_as_uint(v.y);
+        }
+    } else {
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const uint32_t lo = lds_u16(sza[a] + 4 * w);
+                const uint32_t hi = (2 * w + 1 < NG) ? lds_u16(sza[a] + 4 * w + 2) : 0u;
+                sz[a][w] = lo | (hi << 16);
+            }
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty);
+#pragma unroll
+    for (int i = 0; i < NG; ++i) {
+        const uint32_t gi = (uint32_t)(gi0 + gb + i);
+        float v[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) v[a] = (i & 1) ? half_hi(sz[a][i >> 1]) : half_lo(sz[a][i >> 1]);
+        compute_group(acc, wa[i], wb[i], v[0] * wscale, v[1], v[2] * wscale, v[3], t, brow_a + 256u * gi, bact,
+                      c0_a + 8u * gi, c1_a + 8u * gi);
+    }
+}
+
+// A chunk for this warp: wait for it, then take half of its gcv groups
+// (gcv is even: d_model and d_ff are multiples of 256).
 __device__ __forceinline__ void consume_chunk(float (&acc)[4], uint32_t full, uint32_t empty, uint32_t parity,
-                                              uint32_t sa, int gcv, int half, int g, int t, int gi0, uint32_t brow_a,
-                                              uint32_t c0_a, uint32_t c1_a, float wscale, volatile int* abort_flag,
-                                              uint32_t* err) {
+                                              uint32_t sa, uint32_t szs, int gcv, int half, int g, int t, int gi0, uint32_t brow_a,
+                                              uint32_t bact, uint32_t c0_a, uint32_t c1_a, float wscale,
+                                              volatile int* abort_flag, uint32_t* err) {
     const bool ready = tc::mbar_wait(full, parity, abort_flag, err);
-    const int ng = gcv >> 1, gb = half * ng;
     if (!ready) {
         __syncwarp();
         if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty);
         return;
     }
-    for (int i = 0; i < ng; ++i) {
-        GroupA ga;
-        load_group(ga, sa, gb + i, g, t);
-        if (i == ng - 1) {
-            __syncwarp();
-            if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty);
-        }
-        const int gi = gi0 + gb + i;
-        compute_group(acc, ga, t, brow_a + 256u * gi, c0_a + 8u * gi, c1_a + 8u * gi, wscale);
+    const int ng = gcv >> 1, gb = half * ng;
+    switch (ng) {
+        case 4: consume_groups<4>(acc, sa, szs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
+        case 3: consume_groups<3>(acc, sa, szs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
+        case 2: consume_groups<2>(acc, sa, szs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
+        default: consume_groups<1>(acc, sa, szs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
     }
 }
 
@@ -383,13 +434,14 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     const uint32_t sbase = smem_u32(sm);
     Tab& tab = *reinterpret_cast<Tab*>(sm + p.off_tab);
     volatile int* abort_flag = &tab.abort;
-    const uint32_t full0 = sbase + p.off_bars;
-    const uint32_t empty0 = full0 + 8u * NFULL;
+    const uint32_t szbase = sbase + p.off_sz;
+    const uint32_t full0 = sbase + p.off_bars;            // [NQ][NFQ]
+    const uint32_t empty0 = full0 + 8u * (NQ * NFQ);      // [nslot]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = p.T, k = p.k, R = T * k, E = p.E, d = p.d, f = p.f;
     const int Gd = d >> 7, Gf = f >> 7;
     const int G = gridDim.x, cta = blockIdx.x;
-    const int nslot = p.nslot;
+    const int nslot = p.nslot, ns4 = nslot / NQ;
 
     // ------------------------------------------------ phase 0: init, routing
     // Scratch of phase 0 lives in the ring, which is idle until the producers
@@ -402,7 +454,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     int32_t* wpre = reinterpret_cast<int32_t*>(emask + 32);
     if (threadIdx.x == 0) tab.abort = 0;
     if (warp == PRODUCER_WARP) {
-        for (int i = lane; i < NFULL; i += 32) tc::mbar_init(full0 + 8u * i, FULL_ARRIVALS);
+        for (int i = lane; i < NQ * NFQ; i += 32) tc::mbar_init(full0 + 8u * i, FULL_ARRIVALS);
         for (int i = lane; i < nslot; i += 32) tc::mbar_init(empty0 + 8u * i, 2);
         if (lane == 0) {
             tc::fence_mbar_init();
@@ -421,7 +473,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         __syncwarp();
         route_token(lrow, E, k, &tab.ids[warp * k], &tab.w[warp * k]);
     } else if (warp < CW) {
-        // activations -> fp16 in MMA order, plus C1/C2 per (token, group)
+        // activations -> fp16 in MMA order, plus C1/C2 per (token, group); the
+        // C1/C2 row T is zero (B columns without a token)
         const int nthr = (CW - T) * 32, tid = (warp - T) * 32 + lane;
         const int wpr = d >> 3;  // 16-byte words per row (a multiple of 32)
         float2* cx = reinterpret_cast<float2*>(sm + p.off_cx);
@@ -442,9 +495,6 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             const float2 c = halfwarp_sum(word_c1c2(o));
             if ((lane & 15) == 0) cx[t * Gd + (wr >> 4)] = c;
         }
-        // the zero row (index T): columns without a token
-        for (int i = tid; i < (p.xb_stride >> 4); i += nthr)
-            sts128(sbase + p.off_xb + (uint32_t)(T * p.xb_stride) + 16u * i, make_uint4(0, 0, 0, 0));
         for (int i = tid; i < Gd; i += nthr) cx[T * Gd + i] = make_float2(0.f, 0.f);
     }
     __syncthreads();
@@ -523,54 +573,66 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     if (cta == 0 && p.ids_out)
         for (int a = threadIdx.x; a < R; a += NTHREADS) p.ids_out[a] = tab.ids[a];
 
-    // work shares
+    // work shares.  Phase 1: a contiguous share of the tiles (touched expert,
+    // 8 features).  Phase 2: token tok gets the CTAs c with c * T / G == tok and
+    // each of them a contiguous share of tok's units (16 output rows), so a
+    // CTA stages the h rows of one token only.
     const int U = tab.n_uniq;
     const int nfb1 = f >> 3, nrb = d >> 4;
-    const int N1 = U * nfb1, N2 = T * nrb;
-    // (32-bit products: N1 <= 64 * 2048 and N2 <= 8 * 1024, times G < 2^12)
+    const int N1 = U * nfb1;
+    // (32-bit products: N1 <= 64 * 2048 times G < 2^12)
     const int a1 = cta * N1 / G, b1 = (cta + 1) * N1 / G;
-    const int a2 = cta * N2 / G, b2 = (cta + 1) * N2 / G;
-    const int n1 = b1 - a1, n2u = b2 - a2, n2t = n2u * k;
+    const int tok = cta * T / G;
+    const int c_lo = (tok * G + T - 1) / T, c_hi = ((tok + 1) * G + T - 1) / T;
+    const int r_lo = (cta - c_lo) * nrb / (c_hi - c_lo), r_hi = (cta - c_lo + 1) * nrb / (c_hi - c_lo);
+    const int n1 = b1 - a1, n2u = r_hi - r_lo, n2t = n2u * k;
     const int nch1 = ceil_div(Gd, CHUNK_GROUPS), nch2 = ceil_div(Gf, CHUNK_GROUPS);
 
+    // Tiles of either phase go to pairs round-robin (tile i to pair i % NPAIR);
+    // pipeline qp (producer warp PRODUCER_WARP + qp) feeds pairs 2qp and
+    // 2qp + 1, i.e. tiles 8m + 2qp + e (e = 0, 1).  Its chunks are numbered in
+    // issue order: batch m (those two tiles), chunk c of both tiles before
+    // chunk c + 1; phase 2 continues the numbering after phase 1.
+    auto tiles_of = [&](int n, int qp, int e) {
+        const int first = 2 * qp + e;
+        return n > first ? (n - first + NPAIR - 1) / NPAIR : 0;
+    };
+
     // ---------------------------------------------------------- producers
+    // Lane 0 of the pipeline's warp waits until the chunk's slot is empty and
+    // issues the TMA boxes of the codes; then all lanes copy the matching fp16
+    // scales and zeros with 4-byte cp.async.  One warp per pipeline, in
+    // chunk order: a slot's round r is waited on only after its round r - 1
+    // has completed, so every parity wait is exact.
     if (warp >= PRODUCER_WARP) {
-        const uint32_t pw = (uint32_t)(warp - PRODUCER_WARP);
-        // chunk counter q = round * nslot + slot, kept incrementally (no division
-        // in the issue loop: a runtime divide costs tens of dependent instructions)
-        uint32_t q = 0, slot = 0, round = 0;
+        const int qp = warp - PRODUCER_WARP;
+        const uint32_t fullq = full0 + 8u * (uint32_t)(qp * NFQ);
+        const int slot0 = qp * ns4;
+        // chunk number, its slot inside the pipeline and the slot's round, kept
+        // incrementally (a runtime divide costs tens of dependent instructions)
+        uint32_t qq = 0, sl = 0, round = 0;
         bool ok = true;
-        auto advance = [&]() {
-            ++q;
-            if (++slot == (uint32_t)nslot) {
-                slot = 0;
-                ++round;
-            }
-        };
         auto issue = [&](const CUtensorMap* map, int row0, int row1, int chunk, const uint16_t* s_arr,
                          const uint16_t* z_arr, int Gk) {
-            if ((q & (NPROD - 1)) != pw) {  // another producer warp's chunk
-                advance();
-                return;
-            }
-            const uint32_t full = full0 + 8u * (q & (NFULL - 1)), empty = empty0 + 8u * slot;
-            if (round > 0) {
-                // one lane waits and the warp follows its verdict; __syncwarp orders
-                // the consumers' last reads of the slot before any lane's new copies
-                int w = 1;
-                if (lane == 0) w = tc::mbar_wait(empty, (round - 1) & 1u, abort_flag, p.err);
-                w = __shfl_sync(0xffffffffu, w, 0);
-                __syncwarp();
-                if (!w) {
-                    ok = false;
-                    return;
+            const uint32_t full = fullq + 8u * (qq & (NFQ - 1));
+            const uint32_t slot = (uint32_t)slot0 + sl;
+            int w = 1;
+            if (lane == 0) {
+                if (round > 0) w = tc::mbar_wait(empty0 + 8u * slot, (round - 1) & 1u, abort_flag, p.err);
+                if (w) {
+                    const uint32_t dst = sbase + slot * SLOT_CODE;
+                    tc::mbar_arrive_expect_tx(full, SLOT_CODE);
+                    tc::tma_load_3d(dst, map, full, 0, chunk * LINES, row0);
+                    tc::tma_load_3d(dst + BOX_BYTES, map, full, 0, chunk * LINES, row1);
                 }
             }
-            const uint32_t dst = sbase + (uint32_t)slot * SLOT_BYTES;
-            if (lane == 0) {
-                tc::mbar_arrive_expect_tx(full, SLOT_CODE);
-                tc::tma_load_3d(dst, map, full, 0, chunk * LINES, row0);
-                tc::tma_load_3d(dst + BOX_BYTES, map, full, 0, chunk * LINES, row1);
+            // the warp follows lane 0's verdict; __syncwarp orders the wait
+            // before any lane's copies into the slot
+            w = __shfl_sync(0xffffffffu, w, 0);
+            __syncwarp();
+            if (!w) {
+                ok = false;
+                return;
             }
             const int arr = lane >> 4, r = lane & 15;
             const uint16_t* base = arr ? z_arr : s_arr;
@@ -578,56 +640,56 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             const int g0 = chunk * CHUNK_GROUPS;
             const int gcv = min(CHUNK_GROUPS, Gk - g0);
             const uint16_t* src = base + (size_t)grow * Gk + g0;
-            const uint32_t sdst = dst + SLOT_CODE + (uint32_t)(arr * SZ_ARRAY + r * 16);
+            const uint32_t sdst = szbase + slot * SLOT_SZ + (uint32_t)(arr * SZ_ARRAY + r * 16);
             for (int i = 0; i < (gcv >> 1); ++i) cp_async4(sdst + 4u * i, src + 2 * i);
             tc::cp_async_mbar_arrive_noinc(full);
-            advance();
+            ++qq;
+            if (++sl == (uint32_t)ns4) {
+                sl = 0;
+                ++round;
+            }
         };
-        // Issue order: tiles in batches of NPAIR (one per pair); inside a batch,
-        // chunk c of every tile before chunk c + 1, so that every pair has data
-        // in the ring at once (the consumers' chunk numbering follows it).
-        // lane pp < NPAIR holds the first weight row of tile b0 + pp
-        for (int b0 = 0; b0 < n1 && ok; b0 += NPAIR) {
-            const int nb = min(NPAIR, n1 - b0);
+        // lane e < 2 holds the first weight row of tile b + e
+        for (int b = 2 * qp; b < n1 && ok; b += NPAIR) {
+            const int nb = min(2, n1 - b);
             int my_rg = 0;
             if (lane < nb) {
-                const int tau = a1 + b0 + lane, u = tau / nfb1, fb = tau - u * nfb1;
+                const int tau = a1 + b + lane, u = tau / nfb1, fb = tau - u * nfb1;
                 my_rg = tab.uexp[u] * 2 * f + 8 * fb;
             }
             for (int c = 0; c < nch1 && ok; ++c)
-                for (int pp = 0; pp < nb && ok; ++pp) {
-                    const int rg = __shfl_sync(0xffffffffu, my_rg, pp);
+                for (int e = 0; e < nb && ok; ++e) {
+                    const int rg = __shfl_sync(0xffffffffu, my_rg, e);
                     issue(&map13, rg, rg + f, c, p.w13_s, p.w13_z, Gd);
                 }
         }
-        for (int b0 = 0; b0 < n2t && ok; b0 += NPAIR) {
-            const int nb = min(NPAIR, n2t - b0);
+        for (int b = 2 * qp; b < n2t && ok; b += NPAIR) {
+            const int nb = min(2, n2t - b);
             int my_rg = 0;
             if (lane < nb) {
-                const int i2 = b0 + lane, ul = i2 / k, j = i2 - ul * k;
-                const int ups = a2 + ul, t = ups / nrb, rb = ups - t * nrb;
-                my_rg = tab.ids[t * k + j] * d + 16 * rb;
+                const int i2 = b + lane, ul = i2 / k, j = i2 - ul * k;
+                my_rg = tab.ids[tok * k + j] * d + 16 * (r_lo + ul);
             }
             for (int c = 0; c < nch2 && ok; ++c)
-                for (int pp = 0; pp < nb && ok; ++pp) {
-                    const int rg = __shfl_sync(0xffffffffu, my_rg, pp);
+                for (int e = 0; e < nb && ok; ++e) {
+                    const int rg = __shfl_sync(0xffffffffu, my_rg, e);
                     issue(&map2, rg, rg + 8, c, p.w2_s, p.w2_z, Gf);
                 }
         }
-        // drain: the last use of every slot must have landed before the CTA exits
-        // (each warp waits for its own chunks among the last nslot)
-        const uint32_t issued = q;
-        const uint32_t first = issued > (uint32_t)nslot ? issued - (uint32_t)nslot : 0u;
-        for (uint32_t qq = first; qq < issued; ++qq) {
-            if (qq % NPROD != pw) continue;
-            const uint32_t full = full0 + 8u * (qq & (NFULL - 1));
-            const uint32_t par = (qq / NFULL) & 1u;
-            if (tc::mbar_try_wait(full, par)) continue;
+        // drain: the last use of each of the pipeline's slots (TMA bytes and
+        // every lane's copies) must have landed before the CTA exits
+        if (lane == 0) {
+            const uint32_t first = qq > (uint32_t)ns4 ? qq - (uint32_t)ns4 : 0u;
             const uint64_t t0 = globaltimer_ns();
-            while (!tc::mbar_try_wait(full, par)) {
-                if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-                    set_error(p.err, ERRBIT_TIMEOUT);
-                    break;
+            for (uint32_t qx = first; qx < qq; ++qx) {
+                const uint32_t full = fullq + 8u * (qx & (NFQ - 1));
+                const uint32_t par = (qx / NFQ) & 1u;
+                while (!tc::mbar_try_wait(full, par)) {
+                    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                        set_error(p.err, ERRBIT_TIMEOUT);
+                        qx = qq;
+                        break;
+                    }
                 }
             }
         }
@@ -636,7 +698,10 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
 
     // ---------------------------------------------------------- consumers
     const int pair = warp >> 1, half = warp & 1;
+    const int qp = pair >> 1, e = pair & 1;
     const int g = lane >> 2, t4 = lane & 3;
+    const uint32_t fullq = full0 + 8u * (uint32_t)(qp * NFQ);
+    const int slot0 = qp * ns4;
     float* red = reinterpret_cast<float*>(sm + p.off_red);  // [pair][2][32 lanes][4]
     int rcount = 0;
     auto pair_reduce = [&](float (&acc)[4]) {
@@ -652,36 +717,47 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         }
         ++rcount;
     };
+    // the nch chunks of one tile: pipeline chunk numbers qq, qq + nb, ... (nb:
+    // tiles in the tile's batch), slot sl inside the pipeline
+    auto consume_tile = [&](float (&acc)[4], uint32_t qq, int nb, int nch, int Gk, uint32_t brow_a, uint32_t bact,
+                            uint32_t c0_a, uint32_t c1_a, float wscale) {
+        uint32_t sl = qq % (uint32_t)ns4;
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t slot = (uint32_t)slot0 + sl;
+            consume_chunk(acc, fullq + 8u * (qq & (NFQ - 1)), empty0 + 8u * slot, (qq / NFQ) & 1u,
+                          sbase + slot * SLOT_CODE, szbase + slot * SLOT_SZ, min(CHUNK_GROUPS, Gk - c * CHUNK_GROUPS),
+                          half, g, t4, c * CHUNK_GROUPS, brow_a, bact, c0_a, c1_a, wscale, abort_flag, p.err);
+            qq += (uint32_t)nb;
+            sl += (uint32_t)nb;
+            if (sl >= (uint32_t)ns4) sl -= (uint32_t)ns4;
+        }
+    };
     const uint32_t xb = sbase + p.off_xb, cxa = sbase + p.off_cx;
 
     // phase 1: gate_up tiles
-    for (int tl = pair; tl < n1; tl += NPAIR) {
+    for (int tl = pair, m = 0; tl < n1; tl += NPAIR, ++m) {
         const int tau = a1 + tl, u = tau / nfb1, fb = tau - u * nfb1;
         const int cnt = tab.ucnt[u], off = tab.uoff[u];
         const int col = lane >> 2;
-        const int brow = col < cnt ? tab.ptok[off + col] : T;
+        // B columns without a token are not loaded (bact = 0) and read as zero
+        const int brow = col < cnt ? tab.ptok[off + col] : 0;
         const int cr0 = 2 * t4 < cnt ? tab.ptok[off + 2 * t4] : T;
         const int cr1 = 2 * t4 + 1 < cnt ? tab.ptok[off + 2 * t4 + 1] : T;
         const uint32_t brow_a = xb + (uint32_t)(brow * p.xb_stride);
         const uint32_t c0_a = cxa + (uint32_t)(cr0 * Gd * 8), c1_a = cxa + (uint32_t)(cr1 * Gd * 8);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const int b0 = tl - pair, nb = min(NPAIR, n1 - b0);
-        for (int c = 0; c < nch1; ++c) {
-            const uint32_t q = (uint32_t)(b0 * nch1 + c * nb + pair);  // interleaved issue order
-            const int slot = (int)(q % (uint32_t)nslot);
-            consume_chunk(acc, full0 + 8u * (q % NFULL), empty0 + 8u * slot, (q / NFULL) & 1u,
-                          sbase + (uint32_t)slot * SLOT_BYTES, min(CHUNK_GROUPS, Gd - c * CHUNK_GROUPS), half, g,
-                          t4, c * CHUNK_GROUPS, brow_a, c0_a, c1_a, 1.0f, abort_flag, p.err);
-        }
+        const int nb = min(2, n1 - (tl - e));
+        consume_tile(acc, (uint32_t)(2 * m * nch1 + e), nb, nch1, Gd, brow_a, (uint32_t)(col < cnt), c0_a, c1_a,
+                     1.0f);
         pair_reduce(acc);
         if (half == 0 && !*abort_flag) {
             // h = SiLU(gate) * up for feature 8 fb + g and columns 2 t4, 2 t4 + 1
             const uint32_t hoff = staged_offset(8 * fb + g);
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int colm = 2 * t4 + m;
+            for (int mm = 0; mm < 2; ++mm) {
+                const int colm = 2 * t4 + mm;
                 if (colm < cnt) {
-                    const float h = silu(acc[m]) * acc[2 + m];
+                    const float h = silu(acc[mm]) * acc[2 + mm];
                     const __half hh = __float2half_rn(h);
                     if (__hisinf(hh) || __hisnan(hh)) set_error(p.err, ERRBIT_F16_RANGE);
                     *reinterpret_cast<__half*>(p.hb + (size_t)(off + colm) * (f * 2) + hoff) = hh;
@@ -712,27 +788,22 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     }
     bar_sync(1, CONSUMER_THREADS);
 
-    // stage the h rows of this CTA's tokens (<= 2 tokens x k slots) + C1/C2
-    const int tok_lo = n2u > 0 ? a2 / nrb : 0;
-    const int tok_hi = n2u > 0 ? (b2 - 1) / nrb : -1;
-    const int nloc = (tok_hi - tok_lo + 1) * k;  // staged rows; row 2k is the zero row
-    const int zrow = 2 * k;
+    // stage token tok's k rows of h (slot j at row j) and their C1/C2; the
+    // C1/C2 row k is zero
+    const int zrow = k;
     const uint32_t hs = sbase + p.off_hs, cha = sbase + p.off_ch;
     float2* ch = reinterpret_cast<float2*>(sm + p.off_ch);
-    if (!*abort_flag) {
+    if (!*abort_flag && n2u > 0) {
         const int tid = threadIdx.x;
         const int wpr = f >> 3;  // 16-byte words per row, a multiple of 32
-        for (int wi = tid; wi < nloc * wpr; wi += CONSUMER_THREADS) {
+        for (int wi = tid; wi < k * wpr; wi += CONSUMER_THREADS) {
             const int lr = wi / wpr, wr = wi - lr * wpr;
-            const int a = (tok_lo + lr / k) * k + lr % k;
-            const uint4 o = ldg_cg16(p.hb + (size_t)tab.pos[a] * (f * 2) + 16 * (size_t)wr);
+            const uint4 o = ldg_cg16(p.hb + (size_t)tab.pos[tok * k + lr] * (f * 2) + 16 * (size_t)wr);
             sts128(hs + (uint32_t)(lr * p.hs_stride) + 16u * wr, o);
             // a staged word holds one word's 8 values in MMA order (staged_offset)
             const float2 c = halfwarp_sum(word_c1c2(o));
             if ((lane & 15) == 0) ch[lr * Gf + (wr >> 4)] = c;
         }
-        for (int i = tid; i < (p.hs_stride >> 4); i += CONSUMER_THREADS)
-            sts128(hs + (uint32_t)(zrow * p.hs_stride) + 16u * i, make_uint4(0, 0, 0, 0));
         for (int i = tid; i < Gf; i += CONSUMER_THREADS) ch[zrow * Gf + i] = make_float2(0.f, 0.f);
     }
     bar_sync(1, CONSUMER_THREADS);
@@ -740,6 +811,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     // phase 2: down tiles (unit, slot j); one partial per (unit, pair)
     float* red2 = reinterpret_cast<float*>(sm + p.off_red2);  // [unit][pair][16]
     {
+        const uint32_t qbase = (uint32_t)((tiles_of(n1, qp, 0) + tiles_of(n1, qp, 1)) * nch1);
         int cur = -1;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         auto flush = [&](int ul) {
@@ -750,44 +822,33 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
                 dst[g + 8] = acc[2];
             }
         };
-        const uint32_t qbase = (uint32_t)(n1 * nch1);
-        for (int i2 = pair; i2 < n2t; i2 += NPAIR) {
+        const uint32_t bact = (uint32_t)((lane >> 2) == 0);  // column 0 is the token
+        for (int i2 = pair, m = 0; i2 < n2t; i2 += NPAIR, ++m) {
             const int ul = i2 / k, j = i2 - ul * k;
             if (ul != cur) {
                 if (cur >= 0) flush(cur);
                 cur = ul;
                 acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
             }
-            const int ups = a2 + ul, t = ups / nrb;
-            const int a = t * k + j;
-            const float wj = tab.w[a];
-            const int lr = (t - tok_lo) * k + j;
-            const int brow = (lane >> 2) == 0 ? lr : zrow;
-            const int cr0 = t4 == 0 ? lr : zrow;
-            const uint32_t brow_a = hs + (uint32_t)(brow * p.hs_stride);
+            const float wj = tab.w[tok * k + j];
+            const int cr0 = t4 == 0 ? j : zrow;
+            const uint32_t brow_a = hs + (uint32_t)(j * p.hs_stride);
             const uint32_t c0_a = cha + (uint32_t)(cr0 * Gf * 8), c1_a = cha + (uint32_t)(zrow * Gf * 8);
-            const int b0 = i2 - pair, nb = min(NPAIR, n2t - b0);
-            for (int c = 0; c < nch2; ++c) {
-                const uint32_t q = qbase + (uint32_t)(b0 * nch2 + c * nb + pair);  // interleaved issue order
-                const int slot = (int)(q % (uint32_t)nslot);
-                consume_chunk(acc, full0 + 8u * (q % NFULL), empty0 + 8u * slot, (q / NFULL) & 1u,
-                              sbase + (uint32_t)slot * SLOT_BYTES, min(CHUNK_GROUPS, Gf - c * CHUNK_GROUPS), half, g,
-                              t4, c * CHUNK_GROUPS, brow_a, c0_a, c1_a, wj, abort_flag, p.err);
-            }
+            const int nb = min(2, n2t - (i2 - e));
+            consume_tile(acc, qbase + (uint32_t)(2 * m * nch2 + e), nb, nch2, Gf, brow_a, bact, c0_a, c1_a, wj);
         }
         if (cur >= 0) flush(cur);
     }
     bar_sync(1, CONSUMER_THREADS);
 
-    // out[t][16 rb + r] = contributions of the unit's slots, in slot order
+    // out[tok][16 rb + r] = contributions of the unit's slots, in slot order
     if (!*abort_flag) {
         const int nj = min(k, NPAIR);
         for (int idx = threadIdx.x; idx < n2u * 16; idx += CONSUMER_THREADS) {
             const int ul = idx >> 4, r = idx & 15;
-            const int ups = a2 + ul, t = ups / nrb, rb = ups - t * nrb;
             float sum = 0.f;
             for (int j = 0; j < nj; ++j) sum += red2[(ul * NPAIR + (ul * k + j) % NPAIR) * 16 + r];
-            p.out[(size_t)t * d + 16 * rb + r] = float_to_bf16_bits(sum);
+            p.out[(size_t)tok * d + 16 * (r_lo + ul) + r] = float_to_bf16_bits(sum);
         }
     }
 }
@@ -795,17 +856,18 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
 struct Layout {
     int nslot;
     size_t smem;
-    uint32_t off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab, off_cnt;
+    uint32_t off_sz, off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab, off_cnt;
     int xb_stride, hs_stride;
 };
 
 bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
-    if (T < 1 || T > MAX_T || k < 1 || T * k > MAX_R || E < 1 || E > 1024) return false;
+    if (T < 1 || T > MAX_T || k < 1 || T * k > MAX_R || E < 1 || E > 1024 || G < T) return false;
     if (d % 256 || f % 256) return false;
     Layout l{};
     l.xb_stride = 2 * d + ROW_PAD;
     l.hs_stride = 2 * f + ROW_PAD;
-    const int n2u_max = ceil_div(T * (d / 16), G) + 1;
+    // a token has at least G / T CTAs for its d / 16 units
+    const int n2u_max = ceil_div(d / 16, G / T);
     size_t fixed = 0;
     auto take = [&](size_t bytes) {
         const size_t o = fixed;
@@ -815,37 +877,42 @@ bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
     // offsets relative to the end of the ring and its barriers (rebased below).
     // The staged activations (+ C1/C2) are read in phase 1 only and the staged
     // h rows (+ C1/C2) are written after the grid barrier: one shared region.
-    const size_t sx = align_up((size_t)(T + 1) * l.xb_stride, 128) + (size_t)(T + 1) * (d / 128) * 8;
-    const size_t sh = align_up((size_t)(2 * k + 1) * l.hs_stride, 128) + (size_t)(2 * k + 1) * (f / 128) * 8;
+    const size_t sx = align_up((size_t)T * l.xb_stride, 128) + (size_t)(T + 1) * (d / 128) * 8;
+    const size_t sh = align_up((size_t)k * l.hs_stride, 128) + (size_t)(k + 1) * (f / 128) * 8;
     const uint32_t o_xb = take(std::max(sx, sh));
-    const uint32_t o_cx = o_xb + (uint32_t)align_up((size_t)(T + 1) * l.xb_stride, 128);
+    const uint32_t o_cx = o_xb + (uint32_t)align_up((size_t)T * l.xb_stride, 128);
     const uint32_t o_hs = o_xb;
-    const uint32_t o_ch = o_xb + (uint32_t)align_up((size_t)(2 * k + 1) * l.hs_stride, 128);
+    const uint32_t o_ch = o_xb + (uint32_t)align_up((size_t)k * l.hs_stride, 128);
     const uint32_t o_red = take((size_t)NPAIR * 2 * 32 * 4 * 4);
     const uint32_t o_red2 = take((size_t)n2u_max * NPAIR * 16 * 4);
     const uint32_t o_tab = take(sizeof(Tab));
     if (fixed + 1024 >= SMEM_LIMIT) return false;
     const size_t avail = SMEM_LIMIT - 1024 - fixed;
-    int nslot = (int)((avail - 8 * NFULL) / (SLOT_BYTES + 8));
-    nslot = std::min(nslot, 32);
-    if (nslot < MIN_SLOTS) return false;
-    const int nch_max = ceil_div(std::max(d, f) / 128, CHUNK_GROUPS);
-    if (nslot + NPAIR * (nch_max + 1) + 1 > NFULL) return false;
+    const size_t bar_fixed = align_up((size_t)8 * NQ * NFQ + 8 * MAX_SLOTS, 128);
+    if (avail <= bar_fixed) return false;
+    int nslot = (int)((avail - bar_fixed) / (SLOT_CODE + SLOT_SZ));
+    nslot = std::min(nslot, MAX_SLOTS);
+    nslot -= nslot % NQ;
+    // two slots per pipeline at least (a consumer's slot index advances by at
+    // most 2 per chunk), and the full-barrier bound NFQ >= slots + 3
+    if (nslot < 2 * NQ || nslot / NQ + 3 > NFQ) return false;
     // phase-0 scratch in the ring: logits, two count arrays, bitmask, word prefixes
     l.off_cnt = (uint32_t)align_up((size_t)T * E * 4, 16);
-    if (l.off_cnt + (size_t)8 * E + 256 > (size_t)nslot * SLOT_BYTES) return false;
-    const uint32_t ring = (uint32_t)nslot * SLOT_BYTES;
-    const uint32_t bars = (uint32_t)align_up((size_t)8 * (NFULL + nslot), 128);
+    if (l.off_cnt + (size_t)8 * E + 256 > (size_t)nslot * SLOT_CODE) return false;
+    const uint32_t ring = (uint32_t)nslot * SLOT_CODE;
+    const uint32_t szs = (uint32_t)nslot * SLOT_SZ;
+    const uint32_t base = ring + szs + (uint32_t)bar_fixed;
     l.nslot = nslot;
-    l.off_bars = ring;
-    l.off_xb = ring + bars + o_xb;
-    l.off_cx = ring + bars + o_cx;
-    l.off_hs = ring + bars + o_hs;
-    l.off_ch = ring + bars + o_ch;
-    l.off_red = ring + bars + o_red;
-    l.off_red2 = ring + bars + o_red2;
-    l.off_tab = ring + bars + o_tab;
-    l.smem = 1024 + ring + bars + fixed;
+    l.off_sz = ring;
+    l.off_bars = ring + szs;
+    l.off_xb = base + o_xb;
+    l.off_cx = base + o_cx;
+    l.off_hs = base + o_hs;
+    l.off_ch = base + o_ch;
+    l.off_red = base + o_red;
+    l.off_red2 = base + o_red2;
+    l.off_tab = base + o_tab;
+    l.smem = 1024 + base + fixed;
     if (l.smem > SMEM_LIMIT) return false;
     *L = l;
     return true;
@@ -890,6 +957,7 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     p.d = d;
     p.f = f;
     p.nslot = l.nslot;
+    p.off_sz = l.off_sz;
     p.off_bars = l.off_bars;
     p.off_xb = l.off_xb;
     p.off_cx = l.off_cx;
