@@ -70,11 +70,11 @@ constexpr int NTHREADS = 32 * (CW + NQ);
 constexpr int CONSUMER_THREADS = 32 * CW;
 constexpr int LINES = 4;                        // 128-byte lines (2 groups each) per chunk row
 constexpr int CHUNK_GROUPS = 2 * LINES;         // groups of 128 codes per chunk
-constexpr int BOX_BYTES = 8 * LINES * 128;      // one TMA box: 8 rows x 4 lines
-constexpr int SLOT_CODE = 2 * BOX_BYTES;        // 16 rows of codes (a multiple of the 1024-byte swizzle atom)
+constexpr int BOX_BYTES = 8 * LINES * 128;      // 8 rows x 4 lines (rows g; rows g + 8 follow)
+constexpr int SLOT_CODE = 2 * BOX_BYTES;        // one TMA box: 16 rows of codes (a multiple of the 1024-byte swizzle atom)
 constexpr int SZ_ARRAY = 16 * CHUNK_GROUPS * 2; // fp16 [16 rows][8 groups]
 constexpr int SLOT_SZ = 2 * SZ_ARRAY;           // scales, then zeros
-constexpr uint32_t FULL_ARRIVALS = 1 + 32;      // expect_tx arrival + one cp.async arrival per producer lane
+constexpr uint32_t FULL_ARRIVALS = 1;          // lane 0's expect_tx arrival (cp.async arrivals are counted)
 // Each pipeline numbers its chunks in issue order and indexes its "full"
 // barriers by chunk number modulo NFQ (not by ring slot: the pipeline's two
 // pairs consume different chunks, so a pair may wait for chunk q before the
@@ -119,7 +119,16 @@ struct Params {
     uint32_t off_sz, off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab;
     uint32_t off_cnt;          // phase-0 counters inside the ring, after the logits
     int xb_stride, hs_stride;  // bytes per staged row
+    // how the scales and zeros of gate_up / down reach a slot (SZ_*) and their
+    // row stride there in bytes
+    int sz13_mode, sz2_mode, sz13_rs, sz2_rs;
 };
+
+// Scales and zeros of a chunk: by TMA boxes where a row of groups is a
+// multiple of 16 bytes (groups % 8 == 0; [16 rows][8 groups] in the slot), by
+// plain bulk copies where a whole row fits one chunk (the chunk's rows are
+// then contiguous: [16 rows][groups] in the slot), else by 4-byte cp.async.
+enum { SZ_CPASYNC = 0, SZ_TMA = 1, SZ_BULK = 2 };
 
 // ------------------------------------------------------------ small helpers
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
@@ -357,9 +366,9 @@ __device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ush
 // their codes, scales and zeros are copied into registers first and the slot
 // is given back before any math, so a slot is held only for the copy.
 template <int NG>
-__device__ __forceinline__ void consume_groups(float (&acc)[4], uint32_t sa, uint32_t szs, uint32_t empty, int gb,
-                                               int g, int t, int gi0, uint32_t brow_a, uint32_t bact, uint32_t c0_a,
-                                               uint32_t c1_a, float wscale) {
+__device__ __forceinline__ void consume_groups(float (&acc)[4], uint32_t sa, uint32_t szs, uint32_t rs, uint32_t empty,
+                                               int gb, int g, int t, int gi0, uint32_t brow_a, uint32_t bact,
+                                               uint32_t c0_a, uint32_t c1_a, float wscale) {
     uint4 wa[NG], wb[NG];
 #pragma unroll
     for (int i = 0; i < NG; ++i) {
@@ -371,10 +380,11 @@ __device__ __forceinline__ void consume_groups(float (&acc)[4], uint32_t sa, uin
     // (rows g and g + 8), word w holds groups 2w and 2w + 1 of this warp's NG
     constexpr int NW = (NG + 1) / 2;
     uint32_t sz[4][NW];
-    const uint32_t szb = szs + (uint32_t)(gb * 2 + g * 16);
-    const uint32_t sza[4] = {szb, szb + SZ_ARRAY, szb + 128, szb + SZ_ARRAY + 128};
+    const uint32_t szb = szs + (uint32_t)gb * 2 + (uint32_t)g * rs;
+    const uint32_t sza[4] = {szb, szb + SZ_ARRAY, szb + 8 * rs, szb + SZ_ARRAY + 8 * rs};
     if constexpr (NG == 4) {
-        // four groups' values of one row are 8 aligned bytes (gb is 0 or 4)
+        // four groups' values of one row are 8 aligned bytes (gb is 0 or 4;
+        // four groups per warp means 8 per chunk, so rows are 16 bytes)
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const float2 v = lds_f2(sza[a]);
@@ -407,7 +417,7 @@ __device__ __forceinline__ void consume_groups(float (&acc)[4], uint32_t sa, uin
 // A chunk for this warp: wait for it, then take half of its gcv groups
 // (gcv is even: d_model and d_ff are multiples of 256).
 __device__ __forceinline__ void consume_chunk(float (&acc)[4], uint32_t full, uint32_t empty, uint32_t parity,
-                                              uint32_t sa, uint32_t szs, int gcv, int half, int g, int t, int gi0, uint32_t brow_a,
+                                              uint32_t sa, uint32_t szs, uint32_t rs, int gcv, int half, int g, int t, int gi0, uint32_t brow_a,
                                               uint32_t bact, uint32_t c0_a, uint32_t c1_a, float wscale,
                                               volatile int* abort_flag, uint32_t* err) {
     const bool ready = tc::mbar_wait(full, parity, abort_flag, err);
@@ -418,16 +428,18 @@ __device__ __forceinline__ void consume_chunk(float (&acc)[4], uint32_t full, ui
     }
     const int ng = gcv >> 1, gb = half * ng;
     switch (ng) {
-        case 4: consume_groups<4>(acc, sa, szs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
-        case 3: consume_groups<3>(acc, sa, szs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
-        case 2: consume_groups<2>(acc, sa, szs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
-        default: consume_groups<1>(acc, sa, szs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
+        case 4: consume_groups<4>(acc, sa, szs, rs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
+        case 3: consume_groups<3>(acc, sa, szs, rs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
+        case 2: consume_groups<2>(acc, sa, szs, rs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
+        default: consume_groups<1>(acc, sa, szs, rs, empty, gb, g, t, gi0, brow_a, bact, c0_a, c1_a, wscale); break;
     }
 }
 
 // ------------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(NTHREADS, 1)
 decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_constant__ CUtensorMap map2,
+                    const __grid_constant__ CUtensorMap map13s, const __grid_constant__ CUtensorMap map13z,
+                    const __grid_constant__ CUtensorMap map2s, const __grid_constant__ CUtensorMap map2z,
                     const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -460,6 +472,14 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             tc::fence_mbar_init();
             tc::tma_prefetch_desc(&map13);
             tc::tma_prefetch_desc(&map2);
+            if (p.sz13_mode == SZ_TMA) {
+                tc::tma_prefetch_desc(&map13s);
+                tc::tma_prefetch_desc(&map13z);
+            }
+            if (p.sz2_mode == SZ_TMA) {
+                tc::tma_prefetch_desc(&map2s);
+                tc::tma_prefetch_desc(&map2z);
+            }
         }
     } else if (warp == PRODUCER_WARP + 1) {
         for (int i = lane; i < 2 * E; i += 32) cnt_a[i] = 0;
@@ -588,22 +608,26 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     const int n1 = b1 - a1, n2u = r_hi - r_lo, n2t = n2u * k;
     const int nch1 = ceil_div(Gd, CHUNK_GROUPS), nch2 = ceil_div(Gf, CHUNK_GROUPS);
 
-    // Tiles of either phase go to pairs round-robin (tile i to pair i % NPAIR);
-    // pipeline qp (producer warp PRODUCER_WARP + qp) feeds pairs 2qp and
-    // 2qp + 1, i.e. tiles 8m + 2qp + e (e = 0, 1).  Its chunks are numbered in
-    // issue order: batch m (those two tiles), chunk c of both tiles before
-    // chunk c + 1; phase 2 continues the numbering after phase 1.
-    auto tiles_of = [&](int n, int qp, int e) {
-        const int first = 2 * qp + e;
-        return n > first ? (n - first + NPAIR - 1) / NPAIR : 0;
-    };
+    // Work inside the CTA is split by chunks: a phase's W = tiles x chunks per
+    // tile, in (tile, chunk) order, and pair P takes the chunks
+    // [P W / NPAIR, (P + 1) W / NPAIR), so every pair streams the same number
+    // of bytes.  A tile cut by a range boundary leaves partial sums that are
+    // added after the phase (phase 1) or per (unit, pair) (phase 2).
+    // Pipeline qp (producer warp PRODUCER_WARP + qp) feeds pairs 2qp and
+    // 2qp + 1: its chunks are numbered in issue order, chunk i of pair 2qp, then
+    // chunk i of pair 2qp + 1, then i + 1 ...; phase 2 continues after phase 1.
+    auto rng = [](int P, int W) { return P * W / NPAIR; };
+    const int W1 = n1 * nch1, W2 = n2t * nch2;
 
     // ---------------------------------------------------------- producers
-    // Lane 0 of the pipeline's warp waits until the chunk's slot is empty and
-    // issues the TMA boxes of the codes; then all lanes copy the matching fp16
-    // scales and zeros with 4-byte cp.async.  One warp per pipeline, in
-    // chunk order: a slot's round r is waited on only after its round r - 1
-    // has completed, so every parity wait is exact.
+    // Per chunk the pipeline waits until the chunk's slot is empty and issues
+    // the TMA box of the codes.  The fp16 scales and zeros come by TMA as well
+    // where a row's groups are a multiple of 8 (16-byte rows: then one lane
+    // does all of it), else every lane copies its row's values with 4-byte
+    // cp.async and a counted arrival before lane 0 arrives with the byte
+    // count.  One warp per pipeline, in chunk order: a slot's round r is
+    // waited on only after its round r - 1 has completed, so every parity
+    // wait is exact.
     if (warp >= PRODUCER_WARP) {
         const int qp = warp - PRODUCER_WARP;
         const uint32_t fullq = full0 + 8u * (uint32_t)(qp * NFQ);
@@ -611,73 +635,155 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         // chunk number, its slot inside the pipeline and the slot's round, kept
         // incrementally (a runtime divide costs tens of dependent instructions)
         uint32_t qq = 0, sl = 0, round = 0;
-        bool ok = true;
-        auto issue = [&](const CUtensorMap* map, int row0, int row1, int chunk, const uint16_t* s_arr,
-                         const uint16_t* z_arr, int Gk) {
-            const uint32_t full = fullq + 8u * (qq & (NFQ - 1));
-            const uint32_t slot = (uint32_t)slot0 + sl;
-            int w = 1;
-            if (lane == 0) {
-                if (round > 0) w = tc::mbar_wait(empty0 + 8u * slot, (round - 1) & 1u, abort_flag, p.err);
-                if (w) {
-                    const uint32_t dst = sbase + slot * SLOT_CODE;
-                    tc::mbar_arrive_expect_tx(full, SLOT_CODE);
-                    tc::tma_load_3d(dst, map, full, 0, chunk * LINES, row0);
-                    tc::tma_load_3d(dst + BOX_BYTES, map, full, 0, chunk * LINES, row1);
-                }
-            }
-            // the warp follows lane 0's verdict; __syncwarp orders the wait
-            // before any lane's copies into the slot
-            w = __shfl_sync(0xffffffffu, w, 0);
-            __syncwarp();
-            if (!w) {
-                ok = false;
-                return;
-            }
-            const int arr = lane >> 4, r = lane & 15;
-            const uint16_t* base = arr ? z_arr : s_arr;
-            const int grow = r < 8 ? row0 + r : row1 + (r - 8);
-            const int g0 = chunk * CHUNK_GROUPS;
-            const int gcv = min(CHUNK_GROUPS, Gk - g0);
-            const uint16_t* src = base + (size_t)grow * Gk + g0;
-            const uint32_t sdst = szbase + slot * SLOT_SZ + (uint32_t)(arr * SZ_ARRAY + r * 16);
-            for (int i = 0; i < (gcv >> 1); ++i) cp_async4(sdst + 4u * i, src + 2 * i);
-            tc::cp_async_mbar_arrive_noinc(full);
+        int ok = 1;
+        auto advance = [&]() {
             ++qq;
             if (++sl == (uint32_t)ns4) {
                 sl = 0;
                 ++round;
             }
         };
-        // lane e < 2 holds the first weight row of tile b + e
-        for (int b = 2 * qp; b < n1 && ok; b += NPAIR) {
-            const int nb = min(2, n1 - b);
-            int my_rg = 0;
-            if (lane < nb) {
-                const int tau = a1 + b + lane, u = tau / nfb1, fb = tau - u * nfb1;
-                my_rg = tab.uexp[u] * 2 * f + 8 * fb;
+        auto slot_free = [&](uint32_t slot) -> int {
+            return round == 0 || tc::mbar_wait(empty0 + 8u * slot, (round - 1) & 1u, abort_flag, p.err);
+        };
+        // A pair's position in its chunk range: chunk c of tile (p0, p1) =
+        // (touched-expert index, feature block) in phase 1, (unit, slot j) in
+        // phase 2, and the tile's weight rows.  Tiles advance without division.
+        struct Cur {
+            int c, p0, p1, row0, row1, ex, fb8;
+        };
+        auto set_rows = [&](Cur& u, bool up) {
+            if (up) {
+                u.ex = tab.uexp[u.p0];
+                u.fb8 = 8 * u.p1;
+                u.row0 = u.ex * 2 * f + u.fb8;
+                u.row1 = u.row0 + f;
+            } else {
+                u.row0 = tab.ids[tok * k + u.p1] * d + 16 * (r_lo + u.p0);
+                u.row1 = u.row0 + 8;
             }
-            for (int c = 0; c < nch1 && ok; ++c)
-                for (int e = 0; e < nb && ok; ++e) {
-                    const int rg = __shfl_sync(0xffffffffu, my_rg, e);
-                    issue(&map13, rg, rg + f, c, p.w13_s, p.w13_z, Gd);
-                }
-        }
-        for (int b = 2 * qp; b < n2t && ok; b += NPAIR) {
-            const int nb = min(2, n2t - b);
-            int my_rg = 0;
-            if (lane < nb) {
-                const int i2 = b + lane, ul = i2 / k, j = i2 - ul * k;
-                my_rg = tab.ids[tok * k + j] * d + 16 * (r_lo + ul);
+        };
+        auto cur_init = [&](Cur& u, bool up, int x, int nch, bool any) {
+            const int tl = x / nch;
+            u.c = x - tl * nch;
+            const int a = up ? a1 + tl : tl, dv = up ? nfb1 : k;
+            u.p0 = a / dv;
+            u.p1 = a - u.p0 * dv;
+            u.ex = u.fb8 = 0;
+            if (any) set_rows(u, up);
+        };
+        auto cur_next = [&](Cur& u, bool up, int nch, bool more) {
+            if (++u.c < nch) return;
+            u.c = 0;
+            if (++u.p1 == (up ? nfb1 : k)) {
+                u.p1 = 0;
+                ++u.p0;
             }
-            for (int c = 0; c < nch2 && ok; ++c)
-                for (int e = 0; e < nb && ok; ++e) {
-                    const int rg = __shfl_sync(0xffffffffu, my_rg, e);
-                    issue(&map2, rg, rg + 8, c, p.w2_s, p.w2_z, Gf);
+            if (more) set_rows(u, up);
+        };
+        auto tma_codes = [&](bool up, uint32_t dst, uint32_t full, const Cur& u) {
+            if (up)
+                tc::tma_load_4d(dst, &map13, full, 0, u.c * LINES, u.fb8, 2 * u.ex);
+            else
+                tc::tma_load_3d(dst, &map2, full, 0, u.c * LINES, u.row0);
+        };
+        // one phase: the two pairs' chunk ranges interleaved (chunk i of pair
+        // 2qp, then of pair 2qp + 1)
+        auto run = [&](bool up, int W, int nch, int mode, const uint16_t* s_arr, const uint16_t* z_arr, int Gk) {
+            const int xa = rng(2 * qp, W), xm = rng(2 * qp + 1, W), xz = rng(2 * qp + 2, W);
+            const int len[2] = {xm - xa, xz - xm};
+            const int lmax = max(len[0], len[1]);
+            Cur cu[2];
+            cur_init(cu[0], up, xa, nch, len[0] > 0);
+            cur_init(cu[1], up, xm, nch, len[1] > 0);
+            if (mode != SZ_CPASYNC) {
+                // bytes per chunk: codes + two arrays of 16 rows (8 groups by TMA,
+                // all Gk groups by bulk copy)
+                const uint32_t tx = SLOT_CODE + (mode == SZ_TMA ? SLOT_SZ : 64u * (uint32_t)Gk);
+                if (lane == 0) {
+                    for (int i = 0; i < lmax && ok; ++i)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            if (i >= len[e] || !ok) continue;
+                            Cur& u = cu[e];
+                            const uint32_t full = fullq + 8u * (qq & (NFQ - 1));
+                            const uint32_t slot = (uint32_t)slot0 + sl;
+                            ok = slot_free(slot);
+                            if (!ok) break;
+                            const uint32_t dst = sbase + slot * SLOT_CODE, sdst = szbase + slot * SLOT_SZ;
+                            tc::mbar_arrive_expect_tx(full, tx);
+                            tma_codes(up, dst, full, u);
+                            const int g0 = u.c * CHUNK_GROUPS;
+                            if (mode == SZ_TMA) {
+                                if (up) {
+                                    tc::tma_load_3d(sdst, &map13s, full, g0, u.fb8, 2 * u.ex);
+                                    tc::tma_load_3d(sdst + SZ_ARRAY, &map13z, full, g0, u.fb8, 2 * u.ex);
+                                } else {
+                                    tc::tma_load_2d(sdst, &map2s, full, g0, u.row0);
+                                    tc::tma_load_2d(sdst + SZ_ARRAY, &map2z, full, g0, u.row0);
+                                }
+                            } else if (up) {
+                                // 8 gate rows, then 8 up rows, of every group
+                                const uint32_t hb = 16u * (uint32_t)Gk;
+                                tc::bulk_load(sdst, s_arr + (size_t)u.row0 * Gk, hb, full);
+                                tc::bulk_load(sdst + hb, s_arr + (size_t)u.row1 * Gk, hb, full);
+                                tc::bulk_load(sdst + SZ_ARRAY, z_arr + (size_t)u.row0 * Gk, hb, full);
+                                tc::bulk_load(sdst + SZ_ARRAY + hb, z_arr + (size_t)u.row1 * Gk, hb, full);
+                            } else {
+                                tc::bulk_load(sdst, s_arr + (size_t)u.row0 * Gk, 32u * (uint32_t)Gk, full);
+                                tc::bulk_load(sdst + SZ_ARRAY, z_arr + (size_t)u.row0 * Gk, 32u * (uint32_t)Gk, full);
+                            }
+                            advance();
+                            cur_next(u, up, nch, i + 1 < len[e]);
+                        }
                 }
-        }
-        // drain: the last use of each of the pipeline's slots (TMA bytes and
-        // every lane's copies) must have landed before the CTA exits
+                // the other lanes take over lane 0's state
+                qq = __shfl_sync(0xffffffffu, qq, 0);
+                sl = __shfl_sync(0xffffffffu, sl, 0);
+                round = __shfl_sync(0xffffffffu, round, 0);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                return;
+            }
+            const int arr = lane >> 4, r = lane & 15;
+            const uint16_t* base = arr ? z_arr : s_arr;
+            for (int i = 0; i < lmax && ok; ++i)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    if (i >= len[e] || !ok) continue;
+                    Cur& u = cu[e];
+                    const uint32_t full = fullq + 8u * (qq & (NFQ - 1));
+                    const uint32_t slot = (uint32_t)slot0 + sl;
+                    int w = 1;
+                    if (lane == 0) w = slot_free(slot);
+                    // the warp follows lane 0's verdict; __syncwarp orders the
+                    // wait before any lane's copies into the slot
+                    ok = __shfl_sync(0xffffffffu, w, 0);
+                    __syncwarp();
+                    if (!ok) break;
+                    const int grow = r < 8 ? u.row0 + r : u.row1 + (r - 8);
+                    const int g0 = u.c * CHUNK_GROUPS;
+                    const int gcv = min(CHUNK_GROUPS, Gk - g0);
+                    const uint16_t* src = base + (size_t)grow * Gk + g0;
+                    const uint32_t sdst = szbase + slot * SLOT_SZ + (uint32_t)(arr * SZ_ARRAY + r * 16);
+                    for (int gi = 0; gi < (gcv >> 1); ++gi) cp_async4(sdst + 4u * gi, src + 2 * gi);
+                    // counted arrivals first, so the phase cannot complete
+                    // before every lane's copies are tracked
+                    tc::cp_async_mbar_arrive(full);
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc::mbar_arrive_expect_tx(full, SLOT_CODE);
+                        tma_codes(up, sbase + slot * SLOT_CODE, full, u);
+                    }
+                    advance();
+                    cur_next(u, up, nch, i + 1 < len[e]);
+                }
+        };
+        run(true, W1, nch1, p.sz13_mode, p.w13_s, p.w13_z, Gd);
+        if (ok) run(false, W2, nch2, p.sz2_mode, p.w2_s, p.w2_z, Gf);
+        if (p.sz13_mode == SZ_CPASYNC || p.sz2_mode == SZ_CPASYNC)
+            asm volatile("cp.async.wait_all;" ::: "memory");  // this lane's copies have landed
+        // drain: the last use of each of the pipeline's slots must have landed
+        // before the CTA exits
         if (lane == 0) {
             const uint32_t first = qq > (uint32_t)ns4 ? qq - (uint32_t)ns4 : 0u;
             const uint64_t t0 = globaltimer_ns();
@@ -717,52 +823,109 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         }
         ++rcount;
     };
-    // the nch chunks of one tile: pipeline chunk numbers qq, qq + nb, ... (nb:
-    // tiles in the tile's batch), slot sl inside the pipeline
-    auto consume_tile = [&](float (&acc)[4], uint32_t qq, int nb, int nch, int Gk, uint32_t brow_a, uint32_t bact,
-                            uint32_t c0_a, uint32_t c1_a, float wscale) {
-        uint32_t sl = qq % (uint32_t)ns4;
-        for (int c = 0; c < nch; ++c) {
-            const uint32_t slot = (uint32_t)slot0 + sl;
-            consume_chunk(acc, fullq + 8u * (qq & (NFQ - 1)), empty0 + 8u * slot, (qq / NFQ) & 1u,
-                          sbase + slot * SLOT_CODE, szbase + slot * SLOT_SZ, min(CHUNK_GROUPS, Gk - c * CHUNK_GROUPS),
-                          half, g, t4, c * CHUNK_GROUPS, brow_a, bact, c0_a, c1_a, wscale, abort_flag, p.err);
-            qq += (uint32_t)nb;
-            sl += (uint32_t)nb;
-            if (sl >= (uint32_t)ns4) sl -= (uint32_t)ns4;
-        }
+    // This pair's chunks of a phase: pipeline numbers qbase + 2i + e while the
+    // partner pair also has an i-th chunk, then consecutive.  The slot index
+    // inside the pipeline follows incrementally (steps of 1 or 2 <= ns4).
+    struct Seq {
+        uint32_t qq, sl;
+        int i, lmin;
+    };
+    auto seq_start = [&](int W, uint32_t qbase) {
+        const int len_me = rng(pair + 1, W) - rng(pair, W);
+        const int len_pt = e ? rng(pair, W) - rng(pair - 1, W) : rng(pair + 2, W) - rng(pair + 1, W);
+        Seq s;
+        s.lmin = min(len_me, len_pt);
+        s.i = 0;
+        s.qq = qbase + (uint32_t)(s.lmin > 0 ? e : 0);
+        s.sl = s.qq % (uint32_t)ns4;
+        return s;
+    };
+    auto seq_chunk = [&](Seq& s, float (&acc)[4], int c, int Gk, uint32_t rs, uint32_t brow_a, uint32_t bact,
+                         uint32_t c0_a, uint32_t c1_a, float wscale) {
+        const uint32_t slot = (uint32_t)slot0 + s.sl;
+        consume_chunk(acc, fullq + 8u * (s.qq & (NFQ - 1)), empty0 + 8u * slot, (s.qq / NFQ) & 1u,
+                      sbase + slot * SLOT_CODE, szbase + slot * SLOT_SZ, rs, min(CHUNK_GROUPS, Gk - c * CHUNK_GROUPS),
+                      half, g, t4, c * CHUNK_GROUPS, brow_a, bact, c0_a, c1_a, wscale, abort_flag, p.err);
+        ++s.i;
+        const uint32_t step = s.i <= s.lmin - 1 ? 2u : (s.i == s.lmin ? (uint32_t)(2 - e) : 1u);
+        s.qq += step;
+        s.sl += step;
+        if (s.sl >= (uint32_t)ns4) s.sl -= (uint32_t)ns4;
     };
     const uint32_t xb = sbase + p.off_xb, cxa = sbase + p.off_cx;
+    // partial sums of tiles cut by a range boundary: [pair][head, tail][32 lanes][4]
+    // (aliases red2, which is used only after the grid barrier)
+    float* part = reinterpret_cast<float*>(sm + p.off_red2);
 
-    // phase 1: gate_up tiles
-    for (int tl = pair, m = 0; tl < n1; tl += NPAIR, ++m) {
+    // phase 1: gate_up.  h = SiLU(gate) * up of tile tl (half 0 of a pair, from
+    // acc = the pair's sums: rows g (gate) and g + 8 (up), columns 2 t4, 2 t4 + 1)
+    auto h_epilogue = [&](int tl, const float (&acc)[4]) {
         const int tau = a1 + tl, u = tau / nfb1, fb = tau - u * nfb1;
         const int cnt = tab.ucnt[u], off = tab.uoff[u];
-        const int col = lane >> 2;
-        // B columns without a token are not loaded (bact = 0) and read as zero
-        const int brow = col < cnt ? tab.ptok[off + col] : 0;
-        const int cr0 = 2 * t4 < cnt ? tab.ptok[off + 2 * t4] : T;
-        const int cr1 = 2 * t4 + 1 < cnt ? tab.ptok[off + 2 * t4 + 1] : T;
-        const uint32_t brow_a = xb + (uint32_t)(brow * p.xb_stride);
-        const uint32_t c0_a = cxa + (uint32_t)(cr0 * Gd * 8), c1_a = cxa + (uint32_t)(cr1 * Gd * 8);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const int nb = min(2, n1 - (tl - e));
-        consume_tile(acc, (uint32_t)(2 * m * nch1 + e), nb, nch1, Gd, brow_a, (uint32_t)(col < cnt), c0_a, c1_a,
-                     1.0f);
-        pair_reduce(acc);
-        if (half == 0 && !*abort_flag) {
-            // h = SiLU(gate) * up for feature 8 fb + g and columns 2 t4, 2 t4 + 1
-            const uint32_t hoff = staged_offset(8 * fb + g);
+        const uint32_t hoff = staged_offset(8 * fb + g);
 #pragma unroll
-            for (int mm = 0; mm < 2; ++mm) {
-                const int colm = 2 * t4 + mm;
-                if (colm < cnt) {
-                    const float h = silu(acc[mm]) * acc[2 + mm];
-                    const __half hh = __float2half_rn(h);
-                    if (__hisinf(hh) || __hisnan(hh)) set_error(p.err, ERRBIT_F16_RANGE);
-                    *reinterpret_cast<__half*>(p.hb + (size_t)(off + colm) * (f * 2) + hoff) = hh;
+        for (int mm = 0; mm < 2; ++mm) {
+            const int colm = 2 * t4 + mm;
+            if (colm < cnt) {
+                const float h = silu(acc[mm]) * acc[2 + mm];
+                const __half hh = __float2half_rn(h);
+                if (__hisinf(hh) || __hisnan(hh)) set_error(p.err, ERRBIT_F16_RANGE);
+                *reinterpret_cast<__half*>(p.hb + (size_t)(off + colm) * (f * 2) + hoff) = hh;
+            }
+        }
+    };
+    {
+        const int x_lo = rng(pair, W1), x_hi = rng(pair + 1, W1);
+        Seq s = seq_start(W1, 0u);
+        for (int x = x_lo; x < x_hi;) {
+            const int tl = x / nch1, c0 = x - tl * nch1, c1 = min(nch1, c0 + (x_hi - x));
+            const int tau = a1 + tl, u = tau / nfb1;
+            const int cnt = tab.ucnt[u], off = tab.uoff[u];
+            const int col = lane >> 2;
+            // B columns without a token are not loaded (bact = 0) and read as zero
+            const int brow = col < cnt ? tab.ptok[off + col] : 0;
+            const int cr0 = 2 * t4 < cnt ? tab.ptok[off + 2 * t4] : T;
+            const int cr1 = 2 * t4 + 1 < cnt ? tab.ptok[off + 2 * t4 + 1] : T;
+            const uint32_t brow_a = xb + (uint32_t)(brow * p.xb_stride);
+            const uint32_t c0_a = cxa + (uint32_t)(cr0 * Gd * 8), c1_a = cxa + (uint32_t)(cr1 * Gd * 8);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c = c0; c < c1; ++c)
+                seq_chunk(s, acc, c, Gd, (uint32_t)p.sz13_rs, brow_a, (uint32_t)(col < cnt), c0_a, c1_a, 1.0f);
+            pair_reduce(acc);
+            if (half == 0 && !*abort_flag) {
+                if (c0 == 0 && c1 == nch1) {
+                    h_epilogue(tl, acc);
+                } else {
+                    // head piece (the tile began in an earlier range) or tail piece
+                    float* pp = part + ((pair * 2 + (c0 > 0 ? 0 : 1)) * 32 + lane) * 4;
+                    *reinterpret_cast<float4*>(pp) = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 }
             }
+            x += c1 - c0;
+        }
+    }
+    bar_sync(1, CONSUMER_THREADS);
+    // tiles cut by boundaries: the first boundary inside tile tc (that of pair
+    // P = this pair, P >= 1) adds the pieces of the pairs P - 1, P, ... that
+    // hold parts of tc, in pair order, and writes tc's h
+    if (half == 0 && pair >= 1 && !*abort_flag) {
+        const int xbd = rng(pair, W1);
+        const int tc_ = xbd / nch1;
+        if (xbd < W1 && xbd - tc_ * nch1 != 0 && rng(pair - 1, W1) <= tc_ * nch1) {
+            const int tstart = tc_ * nch1, tend = tstart + nch1;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int P2 = pair - 1; P2 < NPAIR; ++P2) {
+                const int s0 = rng(P2, W1), s1 = rng(P2 + 1, W1);
+                if (s0 >= tend) break;
+                if (s1 <= s0) continue;
+                const float4 v =
+                    *reinterpret_cast<const float4*>(part + ((P2 * 2 + (s0 > tstart ? 0 : 1)) * 32 + lane) * 4);
+                acc[0] += v.x;
+                acc[1] += v.y;
+                acc[2] += v.z;
+                acc[3] += v.w;
+            }
+            h_epilogue(tc_, acc);
         }
     }
 
@@ -788,11 +951,12 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     }
     bar_sync(1, CONSUMER_THREADS);
 
-    // stage token tok's k rows of h (slot j at row j) and their C1/C2; the
-    // C1/C2 row k is zero
+    // stage token tok's k rows of h (slot j at row j) and their C1/C2 (the
+    // C1/C2 row k is zero); clear the per-(unit, pair) partials
     const int zrow = k;
     const uint32_t hs = sbase + p.off_hs, cha = sbase + p.off_ch;
     float2* ch = reinterpret_cast<float2*>(sm + p.off_ch);
+    float* red2 = reinterpret_cast<float*>(sm + p.off_red2);  // [unit][pair][16]
     if (!*abort_flag && n2u > 0) {
         const int tid = threadIdx.x;
         const int wpr = f >> 3;  // 16-byte words per row, a multiple of 32
@@ -805,13 +969,15 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             if ((lane & 15) == 0) ch[lr * Gf + (wr >> 4)] = c;
         }
         for (int i = tid; i < Gf; i += CONSUMER_THREADS) ch[zrow * Gf + i] = make_float2(0.f, 0.f);
+        for (int i = tid; i < n2u * NPAIR * 16; i += CONSUMER_THREADS) red2[i] = 0.f;
     }
     bar_sync(1, CONSUMER_THREADS);
 
-    // phase 2: down tiles (unit, slot j); one partial per (unit, pair)
-    float* red2 = reinterpret_cast<float*>(sm + p.off_red2);  // [unit][pair][16]
+    // phase 2: down tiles i2 = (unit ul, slot j); a pair's chunks accumulate
+    // over the slots and K range it holds of a unit, one partial per (unit, pair)
     {
-        const uint32_t qbase = (uint32_t)((tiles_of(n1, qp, 0) + tiles_of(n1, qp, 1)) * nch1);
+        const int x_lo = rng(pair, W2), x_hi = rng(pair + 1, W2);
+        Seq s = seq_start(W2, (uint32_t)(rng(2 * qp + 2, W1) - rng(2 * qp, W1)));
         int cur = -1;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         auto flush = [&](int ul) {
@@ -823,7 +989,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             }
         };
         const uint32_t bact = (uint32_t)((lane >> 2) == 0);  // column 0 is the token
-        for (int i2 = pair, m = 0; i2 < n2t; i2 += NPAIR, ++m) {
+        for (int x = x_lo; x < x_hi;) {
+            const int i2 = x / nch2, c0 = x - i2 * nch2, c1 = min(nch2, c0 + (x_hi - x));
             const int ul = i2 / k, j = i2 - ul * k;
             if (ul != cur) {
                 if (cur >= 0) flush(cur);
@@ -834,20 +1001,20 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             const int cr0 = t4 == 0 ? j : zrow;
             const uint32_t brow_a = hs + (uint32_t)(j * p.hs_stride);
             const uint32_t c0_a = cha + (uint32_t)(cr0 * Gf * 8), c1_a = cha + (uint32_t)(zrow * Gf * 8);
-            const int nb = min(2, n2t - (i2 - e));
-            consume_tile(acc, qbase + (uint32_t)(2 * m * nch2 + e), nb, nch2, Gf, brow_a, bact, c0_a, c1_a, wj);
+            for (int c = c0; c < c1; ++c) seq_chunk(s, acc, c, Gf, (uint32_t)p.sz2_rs, brow_a, bact, c0_a, c1_a, wj);
+            x += c1 - c0;
         }
         if (cur >= 0) flush(cur);
     }
     bar_sync(1, CONSUMER_THREADS);
 
-    // out[tok][16 rb + r] = contributions of the unit's slots, in slot order
+    // out[tok][16 rb + r] = the unit's partials, in pair order
     if (!*abort_flag) {
-        const int nj = min(k, NPAIR);
         for (int idx = threadIdx.x; idx < n2u * 16; idx += CONSUMER_THREADS) {
             const int ul = idx >> 4, r = idx & 15;
             float sum = 0.f;
-            for (int j = 0; j < nj; ++j) sum += red2[(ul * NPAIR + (ul * k + j) % NPAIR) * 16 + r];
+#pragma unroll
+            for (int P2 = 0; P2 < NPAIR; ++P2) sum += red2[(ul * NPAIR + P2) * 16 + r];
             p.out[(size_t)tok * d + 16 * (r_lo + ul) + r] = float_to_bf16_bits(sum);
         }
     }
@@ -862,7 +1029,7 @@ struct Layout {
 
 bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
     if (T < 1 || T > MAX_T || k < 1 || T * k > MAX_R || E < 1 || E > 1024 || G < T) return false;
-    if (d % 256 || f % 256) return false;
+    if (d % 256 || f % 256 || f >= 65536) return false;  // (a feature index is packed in 16 bits)
     Layout l{};
     l.xb_stride = 2 * d + ROW_PAD;
     l.hs_stride = 2 * f + ROW_PAD;
@@ -884,7 +1051,8 @@ bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
     const uint32_t o_hs = o_xb;
     const uint32_t o_ch = o_xb + (uint32_t)align_up((size_t)k * l.hs_stride, 128);
     const uint32_t o_red = take((size_t)NPAIR * 2 * 32 * 4 * 4);
-    const uint32_t o_red2 = take((size_t)n2u_max * NPAIR * 16 * 4);
+    // red2 (phase 2) also holds phase 1's cut-tile pieces [pair][2][32][4]
+    const uint32_t o_red2 = take(std::max((size_t)n2u_max * NPAIR * 16 * 4, (size_t)NPAIR * 2 * 32 * 4 * 4));
     const uint32_t o_tab = take(sizeof(Tab));
     if (fixed + 1024 >= SMEM_LIMIT) return false;
     const size_t avail = SMEM_LIMIT - 1024 - fixed;
@@ -931,13 +1099,34 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     const int G = num_sms();
     Layout l;
     if (!plan_layout(in.T, in.k, E, d, f, G, &l)) return cudaErrorInvalidValue;
-    // codes viewed as [rows][lines of 32 words][32 words]
+    // codes as 32-word lines: gate_up [expert * 2 + (gate, up)][feature][line][32
+    // words], box 8 features of both halves; down [row][line][32 words], box 16 rows
     CUtensorMap m13, m2;
-    if (!make_tensor_map_3d(&m13, W.w13_q, 32, (uint64_t)d / 256, (uint64_t)E * 2 * f, 128, (uint64_t)d / 2, 32,
-                            LINES, 8))
+    const uint64_t d13[4] = {32, (uint64_t)d / 256, (uint64_t)f, (uint64_t)E * 2};
+    const uint64_t s13[3] = {128, (uint64_t)d / 2, (uint64_t)f * d / 2};
+    const uint32_t b13[4] = {32, LINES, 8, 2};
+    if (!make_tensor_map_u32(&m13, W.w13_q, 4, d13, s13, b13)) return cudaErrorInvalidValue;
+    if (!make_tensor_map_3d(&m2, W.w2_q, 32, (uint64_t)f / 256, (uint64_t)E * d, 128, (uint64_t)f / 2, 32, LINES, 16))
         return cudaErrorInvalidValue;
-    if (!make_tensor_map_3d(&m2, W.w2_q, 32, (uint64_t)f / 256, (uint64_t)E * d, 128, (uint64_t)f / 2, 32, LINES, 8))
-        return cudaErrorInvalidValue;
+    // fp16 scales and zeros [rows][groups]: by TMA when a row is a multiple of
+    // 16 bytes (groups % 8 == 0): gate_up {groups, feature, expert * 2 + half}
+    // box {8, 8, 2}, down {groups, row} box {8, 16}; by bulk copies when a row
+    // fits one chunk (groups < 8; 16-byte aligned arrays); else with cp.async
+    CUtensorMap m13s = m13, m13z = m13, m2s = m2, m2z = m2;
+    const uint64_t Gd = (uint64_t)d / 128, Gf = (uint64_t)f / 128;
+    bool sz13 = Gd % 8 == 0, sz2 = Gf % 8 == 0;
+    auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+    if (sz13) {
+        const uint64_t dims[3] = {Gd, (uint64_t)f, (uint64_t)E * 2}, str[2] = {Gd * 2, (uint64_t)f * Gd * 2};
+        const uint32_t box[3] = {CHUNK_GROUPS, 8, 2};
+        sz13 = make_tensor_map_u16(&m13s, W.w13_s, 3, dims, str, box) &&
+               make_tensor_map_u16(&m13z, W.w13_z, 3, dims, str, box);
+    }
+    if (sz2) {
+        const uint64_t dims[2] = {Gf, (uint64_t)E * d}, str[1] = {Gf * 2};
+        const uint32_t box[2] = {CHUNK_GROUPS, 16};
+        sz2 = make_tensor_map_u16(&m2s, W.w2_s, 2, dims, str, box) && make_tensor_map_u16(&m2z, W.w2_z, 2, dims, str, box);
+    }
     Params p{};
     p.x = in.x;
     p.logits = in.logits;
@@ -969,6 +1158,12 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     p.off_cnt = l.off_cnt;
     p.xb_stride = l.xb_stride;
     p.hs_stride = l.hs_stride;
+    const bool bulk13 = Gd < CHUNK_GROUPS && a16(W.w13_s) && a16(W.w13_z);
+    const bool bulk2 = Gf < CHUNK_GROUPS && a16(W.w2_s) && a16(W.w2_z);
+    p.sz13_mode = sz13 ? SZ_TMA : (bulk13 ? SZ_BULK : SZ_CPASYNC);
+    p.sz2_mode = sz2 ? SZ_TMA : (bulk2 ? SZ_BULK : SZ_CPASYNC);
+    p.sz13_rs = p.sz13_mode == SZ_BULK ? (int)Gd * 2 : 16;
+    p.sz2_rs = p.sz2_mode == SZ_BULK ? (int)Gf * 2 : 16;
 
     static bool configured = false;
     if (!configured) {
@@ -987,7 +1182,7 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, m13, m2, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, m13, m2, m13s, m13z, m2s, m2z, p);
     note_launch();
     return e;
 }

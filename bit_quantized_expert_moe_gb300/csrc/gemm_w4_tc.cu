@@ -476,17 +476,45 @@ constexpr size_t TC_SMEM_LIMIT = 232448;
 
 }  // namespace
 
-bool make_tensor_map_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
-                        uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+bool make_tensor_map_u32(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                         const uint32_t* box) {
     EncodeFn enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {s1, s2};
-    cuuint32_t box[3] = {b0, b1, b2};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+    if (!enc || rank < 1 || rank > 5) return false;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) gs[i] = strides[i];
+    }
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, (cuuint32_t)rank, const_cast<void*>(ptr), gd, gs, bx, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tensor_map_u16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                         const uint32_t* box) {
+    EncodeFn enc = get_encode();
+    if (!enc || rank < 1 || rank > 5) return false;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) gs[i] = strides[i];
+    }
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, (cuuint32_t)rank, const_cast<void*>(ptr), gd, gs, bx, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tensor_map_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                        uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    const uint64_t dims[3] = {d0, d1, d2}, strides[2] = {s1, s2};
+    const uint32_t box[3] = {b0, b1, b2};
+    return make_tensor_map_u32(m, ptr, 3, dims, strides, box);
 }
 
 int tc_max_tiles(int R, int E) { return ceil_div(R, TILE_ROWS) + std::min(R, E); }

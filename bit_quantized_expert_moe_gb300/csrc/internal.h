@@ -121,6 +121,13 @@ cudaError_t launch_tc_down(int E, int d, int f, int R, const TcIn& in, cudaStrea
 // strides s1 (dim 1) and s2 (dim 2), box {b0, b1, b2}, 128-byte swizzle.
 bool make_tensor_map_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
                         uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
+// Tensor map of rank 1..5 over 32-bit words: dims[0] contiguous, strides[i]
+// the byte stride of dimension i + 1, box per dimension, 128-byte swizzle.
+bool make_tensor_map_u32(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                         const uint32_t* box);
+// The same over 16-bit elements, without swizzle.
+bool make_tensor_map_u16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                         const uint32_t* box);
 
 // ----------------------------------------------------------- device info
 int num_sms();

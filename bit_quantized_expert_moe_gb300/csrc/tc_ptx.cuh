@@ -105,6 +105,32 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z) : "memory");
 }
 
+// 4D tiled load of box at (x, y, z, w) into shared memory, completing the
+// box's bytes of transaction count on mbarrier `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];"
+        :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+// Plain bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global memory into shared memory, completing that many bytes
+// of transaction count on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// Counted asynchronous arrival: raises `bar`'s pending count by one now and
+// arrives (lowering it again) once every cp.async issued so far by this thread
+// has landed, so the barrier's expected count does not include it.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+
 // Arrive on `bar` once every cp.async issued so far by this thread has landed
 // (the arrival is not pre-counted: the barrier's expected count includes it).
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
