@@ -54,6 +54,7 @@
 #include <cfloat>
 #include <climits>
 
+#include "fastdiv.h"
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -122,6 +123,11 @@ struct Params {
     // how the scales and zeros of gate_up / down reach a slot (SZ_*) and their
     // row stride there in bytes
     int sz13_mode, sz2_mode, sz13_rs, sz2_rs;
+    // divisors fixed per launch (grid size, tokens, the two CTA counts a token
+    // can have, chunks per tile of each phase, feature blocks, top-k, slots
+    // per pipeline), for division without a runtime divide
+    FastDiv fd_G, fd_T, fd_nct0, fd_nct1, fd_nch1, fd_nch2, fd_nfb1, fd_k, fd_ns4;
+    FastDiv fd_xw, fd_hw;  // 16-byte words per activation row (d / 8) and per h row (f / 8)
 };
 
 // Scales and zeros of a chunk: by TMA boxes where a row of groups is a
@@ -499,7 +505,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         const int wpr = d >> 3;  // 16-byte words per row (a multiple of 32)
         float2* cx = reinterpret_cast<float2*>(sm + p.off_cx);
         for (int wi = tid; wi < T * wpr; wi += nthr) {
-            const int t = wi / wpr, wr = wi - t * wpr;
+            const int t = (int)fd_div((uint32_t)wi, p.fd_xw), wr = wi - t * wpr;
             const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * d) + wr);
             const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
             uint32_t q[4];
@@ -580,12 +586,12 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         if (v0) {
             const int pos = tab.uoff[uidx(e0)] + __popc(m0 & lt);
             tab.pos[a0] = pos;
-            tab.ptok[pos] = a0 / k;
+            tab.ptok[pos] = (int)fd_div((uint32_t)a0, p.fd_k);
         }
         if (v1) {
             const int pos = tab.uoff[uidx(e1)] + cnt_a[e1] + __popc(m1 & lt);
             tab.pos[a1] = pos;
-            tab.ptok[pos] = a1 / k;
+            tab.ptok[pos] = (int)fd_div((uint32_t)a1, p.fd_k);
         }
         if (lane == 0) tab.n_uniq = U;
     }
@@ -601,10 +607,13 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     const int nfb1 = f >> 3, nrb = d >> 4;
     const int N1 = U * nfb1;
     // (32-bit products: N1 <= 64 * 2048 times G < 2^12)
-    const int a1 = cta * N1 / G, b1 = (cta + 1) * N1 / G;
-    const int tok = cta * T / G;
-    const int c_lo = (tok * G + T - 1) / T, c_hi = ((tok + 1) * G + T - 1) / T;
-    const int r_lo = (cta - c_lo) * nrb / (c_hi - c_lo), r_hi = (cta - c_lo + 1) * nrb / (c_hi - c_lo);
+    const int a1 = (int)fd_div((uint32_t)(cta * N1), p.fd_G), b1 = (int)fd_div((uint32_t)((cta + 1) * N1), p.fd_G);
+    const int tok = (int)fd_div((uint32_t)(cta * T), p.fd_G);
+    const int c_lo = (int)fd_div((uint32_t)(tok * G + T - 1), p.fd_T);
+    const int c_hi = (int)fd_div((uint32_t)((tok + 1) * G + T - 1), p.fd_T);
+    const FastDiv fd_nct = (uint32_t)(c_hi - c_lo) == p.fd_nct0.d ? p.fd_nct0 : p.fd_nct1;
+    const int r_lo = (int)fd_div((uint32_t)((cta - c_lo) * nrb), fd_nct);
+    const int r_hi = (int)fd_div((uint32_t)((cta - c_lo + 1) * nrb), fd_nct);
     const int n1 = b1 - a1, n2u = r_hi - r_lo, n2t = n2u * k;
     const int nch1 = ceil_div(Gd, CHUNK_GROUPS), nch2 = ceil_div(Gf, CHUNK_GROUPS);
 
@@ -664,11 +673,12 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             }
         };
         auto cur_init = [&](Cur& u, bool up, int x, int nch, bool any) {
-            const int tl = x / nch;
+            const int tl = (int)fd_div((uint32_t)x, up ? p.fd_nch1 : p.fd_nch2);
             u.c = x - tl * nch;
-            const int a = up ? a1 + tl : tl, dv = up ? nfb1 : k;
-            u.p0 = a / dv;
-            u.p1 = a - u.p0 * dv;
+            const int a = up ? a1 + tl : tl;
+            const FastDiv dv = up ? p.fd_nfb1 : p.fd_k;
+            u.p0 = (int)fd_div((uint32_t)a, dv);
+            u.p1 = a - u.p0 * (int)dv.d;
             u.ex = u.fb8 = 0;
             if (any) set_rows(u, up);
         };
@@ -837,7 +847,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         s.lmin = min(len_me, len_pt);
         s.i = 0;
         s.qq = qbase + (uint32_t)(s.lmin > 0 ? e : 0);
-        s.sl = s.qq % (uint32_t)ns4;
+        s.sl = s.qq - fd_div(s.qq, p.fd_ns4) * (uint32_t)ns4;
         return s;
     };
     auto seq_chunk = [&](Seq& s, float (&acc)[4], int c, int Gk, uint32_t rs, uint32_t brow_a, uint32_t bact,
@@ -860,7 +870,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     // phase 1: gate_up.  h = SiLU(gate) * up of tile tl (half 0 of a pair, from
     // acc = the pair's sums: rows g (gate) and g + 8 (up), columns 2 t4, 2 t4 + 1)
     auto h_epilogue = [&](int tl, const float (&acc)[4]) {
-        const int tau = a1 + tl, u = tau / nfb1, fb = tau - u * nfb1;
+        const int tau = a1 + tl, u = (int)fd_div((uint32_t)tau, p.fd_nfb1), fb = tau - u * nfb1;
         const int cnt = tab.ucnt[u], off = tab.uoff[u];
         const uint32_t hoff = staged_offset(8 * fb + g);
 #pragma unroll
@@ -878,8 +888,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         const int x_lo = rng(pair, W1), x_hi = rng(pair + 1, W1);
         Seq s = seq_start(W1, 0u);
         for (int x = x_lo; x < x_hi;) {
-            const int tl = x / nch1, c0 = x - tl * nch1, c1 = min(nch1, c0 + (x_hi - x));
-            const int tau = a1 + tl, u = tau / nfb1;
+            const int tl = (int)fd_div((uint32_t)x, p.fd_nch1), c0 = x - tl * nch1, c1 = min(nch1, c0 + (x_hi - x));
+            const int tau = a1 + tl, u = (int)fd_div((uint32_t)tau, p.fd_nfb1);
             const int cnt = tab.ucnt[u], off = tab.uoff[u];
             const int col = lane >> 2;
             // B columns without a token are not loaded (bact = 0) and read as zero
@@ -910,7 +920,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     // hold parts of tc, in pair order, and writes tc's h
     if (half == 0 && pair >= 1 && !*abort_flag) {
         const int xbd = rng(pair, W1);
-        const int tc_ = xbd / nch1;
+        const int tc_ = (int)fd_div((uint32_t)xbd, p.fd_nch1);
         if (xbd < W1 && xbd - tc_ * nch1 != 0 && rng(pair - 1, W1) <= tc_ * nch1) {
             const int tstart = tc_ * nch1, tend = tstart + nch1;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -961,7 +971,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         const int tid = threadIdx.x;
         const int wpr = f >> 3;  // 16-byte words per row, a multiple of 32
         for (int wi = tid; wi < k * wpr; wi += CONSUMER_THREADS) {
-            const int lr = wi / wpr, wr = wi - lr * wpr;
+            const int lr = (int)fd_div((uint32_t)wi, p.fd_hw), wr = wi - lr * wpr;
             const uint4 o = ldg_cg16(p.hb + (size_t)tab.pos[tok * k + lr] * (f * 2) + 16 * (size_t)wr);
             sts128(hs + (uint32_t)(lr * p.hs_stride) + 16u * wr, o);
             // a staged word holds one word's 8 values in MMA order (staged_offset)
@@ -990,8 +1000,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         };
         const uint32_t bact = (uint32_t)((lane >> 2) == 0);  // column 0 is the token
         for (int x = x_lo; x < x_hi;) {
-            const int i2 = x / nch2, c0 = x - i2 * nch2, c1 = min(nch2, c0 + (x_hi - x));
-            const int ul = i2 / k, j = i2 - ul * k;
+            const int i2 = (int)fd_div((uint32_t)x, p.fd_nch2), c0 = x - i2 * nch2, c1 = min(nch2, c0 + (x_hi - x));
+            const int ul = (int)fd_div((uint32_t)i2, p.fd_k), j = i2 - ul * k;
             if (ul != cur) {
                 if (cur >= 0) flush(cur);
                 cur = ul;
@@ -1163,6 +1173,17 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     p.sz13_mode = sz13 ? SZ_TMA : (bulk13 ? SZ_BULK : SZ_CPASYNC);
     p.sz2_mode = sz2 ? SZ_TMA : (bulk2 ? SZ_BULK : SZ_CPASYNC);
     p.sz13_rs = p.sz13_mode == SZ_BULK ? (int)Gd * 2 : 16;
+    p.fd_G = make_fastdiv((uint32_t)G);
+    p.fd_T = make_fastdiv((uint32_t)in.T);
+    p.fd_nct0 = make_fastdiv((uint32_t)(G / in.T));
+    p.fd_nct1 = make_fastdiv((uint32_t)(G / in.T + 1));
+    p.fd_nch1 = make_fastdiv((uint32_t)ceil_div(d / 128, CHUNK_GROUPS));
+    p.fd_nch2 = make_fastdiv((uint32_t)ceil_div(f / 128, CHUNK_GROUPS));
+    p.fd_nfb1 = make_fastdiv((uint32_t)(f / 8));
+    p.fd_k = make_fastdiv((uint32_t)in.k);
+    p.fd_ns4 = make_fastdiv((uint32_t)(l.nslot / NQ));
+    p.fd_xw = make_fastdiv((uint32_t)(d / 8));
+    p.fd_hw = make_fastdiv((uint32_t)(f / 8));
     p.sz2_rs = p.sz2_mode == SZ_BULK ? (int)Gf * 2 : 16;
 
     static bool configured = false;
