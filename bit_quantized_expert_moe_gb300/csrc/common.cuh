@@ -83,6 +83,35 @@ __device__ __forceinline__ void nib8_magic(uint32_t w, float2 (&p)[4]) {
                        __uint_as_float(lop_mask_or(wt, 0x000F0000u, ONE)));  // codes 7, 0
 }
 
+// fp16 operands of the int4 GEMMs keep K in groups of 8 interleaved as
+// (0, 4, 1, 5, 2, 6, 3, 7): the order in which masking one packed word of 8
+// codes yields them (nibbles 0 and 4, 1 and 5 of a word, then of the word
+// shifted by 8).  A dot product is unchanged when both operands share the
+// permutation.  Eight fp16 values in natural order as four f16x2 registers
+// (v0,v1), (v2,v3), (v4,v5), (v6,v7) -> (v0,v4), (v1,v5), (v2,v6), (v3,v7).
+__device__ __forceinline__ uint4 k8_interleave(uint32_t p01, uint32_t p23, uint32_t p45, uint32_t p67) {
+    uint4 o;
+    o.x = __byte_perm(p01, p45, 0x5410);
+    o.y = __byte_perm(p01, p45, 0x7632);
+    o.z = __byte_perm(p23, p67, 0x5410);
+    o.w = __byte_perm(p23, p67, 0x7632);
+    return o;
+}
+// Position of element k (0..7) of a group of 8 in that order.
+__device__ __forceinline__ int k8_pos(int k) { return k < 4 ? 2 * k : 2 * k - 7; }
+
+// f16x2 arithmetic on raw 32-bit registers (round to nearest even).
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
 // Packed fp32x2 fused multiply-add (Blackwell FFMA2): d = a * b + c lane-wise.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     unsigned long long ra, rb, rc, rd;

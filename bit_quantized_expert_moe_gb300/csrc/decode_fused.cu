@@ -284,21 +284,9 @@ __device__ __forceinline__ int stage_word(int w) { return (w & 12) | ((w ^ (w >>
 // (256 bytes), word (c/8)%16 at stage_word, then the eight values of the word
 // in the order 0,4,1,5,2,6,3,7 (the k-pairs of the MMA's B fragment).
 __device__ __forceinline__ uint32_t staged_offset(int c) {
-    const int i = c & 7;
-    const int pos = (i < 4) ? 2 * i : 2 * (i - 4) + 1;
-    return (uint32_t)((c >> 7) * 256 + stage_word((c >> 3) & 15) * 16 + pos * 2);
+    return (uint32_t)((c >> 7) * 256 + stage_word((c >> 3) & 15) * 16 + k8_pos(c & 7) * 2);
 }
 
-// Eight fp16 values in natural order (four f16x2 registers (v0,v1), (v2,v3),
-// (v4,v5), (v6,v7)) -> the staged word: (v0,v4), (v1,v5), (v2,v6), (v3,v7).
-__device__ __forceinline__ uint4 to_mma_order(uint32_t p01, uint32_t p23, uint32_t p45, uint32_t p67) {
-    uint4 o;
-    o.x = __byte_perm(p01, p45, 0x5410);
-    o.y = __byte_perm(p01, p45, 0x7632);
-    o.z = __byte_perm(p23, p67, 0x5410);
-    o.w = __byte_perm(p23, p67, 0x7632);
-    return o;
-}
 // A staged word's contributions to (C1, C2).
 __device__ __forceinline__ float2 word_c1c2(uint4 o) {
     const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&o.x));
@@ -516,7 +504,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
                 bad |= f16x2_nonfinite(q[m]);
             }
             if (bad) set_error(p.err, ERRBIT_F16_RANGE);
-            const uint4 o = to_mma_order(q[0], q[1], q[2], q[3]);
+            const uint4 o = k8_interleave(q[0], q[1], q[2], q[3]);
             sts128(sbase + p.off_xb + (uint32_t)(t * p.xb_stride) + staged_offset(wr * 8), o);
             const float2 c = halfwarp_sum(word_c1c2(o));
             if ((lane & 15) == 0) cx[t * Gd + (wr >> 4)] = c;

@@ -12,8 +12,10 @@
 //   A = dequantised weights (fp16, written by the dequant warps, SW128 K-major)
 //   B = activation rows of one expert segment (fp16, TMA, SW128 K-major)
 // The operands are fp16 rather than bf16: bf16 activations convert to fp16
-// exactly inside fp16's range, and (q - z) * s rounds to fp16 with 8x less
-// error than to bf16; values outside fp16's range set the error word.
+// exactly inside fp16's range (values outside set the error word), and a
+// weight is q s - fl16(z s) rounded once to fp16, which keeps 3 more bits than
+// bf16 would.  Both operands hold K interleaved in groups of 8 (k8_interleave),
+// the order in which the dequantisation takes a packed word apart.
 // A work item is (token tile of one expert, block of 128 weight rows); a
 // persistent CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...
 //
@@ -276,7 +278,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 r_it[it] = dw * 16 + it * 4 + (lane >> 3);
                 prow[it] = a_packed_row<GATEUP>(r_it[it]);
             }
-            float2 sc[4], cc[4];  // per row: (s*2^11, s*2^7), (-(2^11+z)s, -(2^7+z)s)
+            uint32_t s2[4], nzs2[4];  // per row, as f16x2: (s, s) and (-fl16(z s), -fl16(z s))
             for (int kc = 0; kc < NK; ++kc) {
                 ok = tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err);
                 ok = __all_sync(0xffffffffu, ok);
@@ -286,28 +288,31 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
 #pragma unroll
                     for (int it = 0; it < 4; ++it) {
                         const size_t si = ((size_t)sbuf * BM + r_it[it]) * G + g;
-                        const float s = half_bits_to_float(sScale[si]);
-                        const float z = half_bits_to_float(sZero[si]);
-                        sc[it] = make_float2(s * 2048.f, s * 128.f);
-                        cc[it] = make_float2(-(2048.f + z) * s, -(128.f + z) * s);
+                        const uint32_t sb = sScale[si];
+                        const float zs = half_bits_to_float((uint16_t)sb) * half_bits_to_float(sZero[si]);
+                        s2[it] = sb * 0x10001u;
+                        nzs2[it] = (uint32_t)float_to_f16_bits(-zs) * 0x10001u;
                     }
                 }
                 const uint32_t* pk = reinterpret_cast<const uint32_t*>(gbase + (sP - base) + stage * P_BYTES);
                 const uint32_t a0 = sA + stage * A_BYTES;
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {
+                    // the 8 codes of one word in the operand order (k0,k4) (k1,k5)
+                    // (k2,k6) (k3,k7): masking a nibble into the mantissa of
+                    // 1024.0 (bits 0-3) or 64.0 (bits 4-7) gives 1024 + q or
+                    // 64 + q exactly, minus the base gives q exactly, and one
+                    // fma gives q s - fl16(z s) rounded once
                     const uint32_t word = pk[prow[it] * 8 + w];
-                    float2 v[4];
-                    nib8_magic(word, v);
-                    // v[m] = (odd code, even code) for pairs (3,4), (1,2), (5,6), (7,0)
-                    const float2 q34 = ffma2(v[0], sc[it], cc[it]);
-                    const float2 q12 = ffma2(v[1], sc[it], cc[it]);
-                    const float2 q56 = ffma2(v[2], sc[it], cc[it]);
-                    const float2 q70 = ffma2(v[3], sc[it], cc[it]);
-                    const uint32_t o0 = pack_f16x2(q70.y, q12.x);  // k0, k1
-                    const uint32_t o1 = pack_f16x2(q12.y, q34.x);  // k2, k3
-                    const uint32_t o2 = pack_f16x2(q34.y, q56.x);  // k4, k5
-                    const uint32_t o3 = pack_f16x2(q56.y, q70.x);  // k6, k7
+                    const uint32_t ws = word >> 8;
+                    const uint32_t o0 = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x000F000Fu, 0x64006400u), 0x64006400u),
+                                                  s2[it], nzs2[it]);
+                    const uint32_t o1 = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x00F000F0u, 0x54005400u), 0x54005400u),
+                                                  s2[it], nzs2[it]);
+                    const uint32_t o2 = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x000F000Fu, 0x64006400u), 0x64006400u),
+                                                  s2[it], nzs2[it]);
+                    const uint32_t o3 = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x00F000F0u, 0x54005400u), 0x54005400u),
+                                                  s2[it], nzs2[it]);
                     const int r = r_it[it];
                     const uint32_t dst = a0 + (r >> 3) * 1024 + (r & 7) * 128 + ((w ^ (r & 7)) << 4);
                     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
@@ -343,6 +348,8 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 if (GATEUP) {
                     const bool lo_half = lane < 16;
                     const int feat = fb * 64 + 16 * q + (lane & 15);
+                    // h is the down GEMM's operand: K interleaved in groups of 8
+                    const int hcol = (feat & ~7) | k8_pos(feat & 7);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const uint32_t send = lo_half ? v[16 + j] : v[j];
@@ -353,7 +360,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                         const uint16_t hb = float_to_f16_bits(silu(g) * u);
                         const bool valid = col < nrows;  // later columns hold the next expert's rows
                         bad |= valid & ((hb & 0x7C00u) == 0x7C00u);
-                        if (valid) p.out[(size_t)(row0 + col) * p.out_ld + feat] = hb;
+                        if (valid) p.out[(size_t)(row0 + col) * p.out_ld + hcol] = hb;
                     }
                 } else {
                     const int feat = fb * BM + 32 * q + lane;

@@ -34,7 +34,8 @@ struct AlignOut {
     Tile* tiles;        // [R/TILE_ROWS + E]
     DevPlan* plan;      // n_uniq, n_tiles
     uint16_t* x_perm;   // [R][d] or null
-    int x_perm_f16;     // 1: write x_perm as fp16 (values outside fp16 set the error word)
+    int x_perm_f16;     // 1: write x_perm as fp16 in the tensor-core operand order (K interleaved
+                        //    in groups of 8, k8_interleave); values outside fp16 set the error word
     int32_t* blockcnt;  // [nblocks][E] scratch for the multi-block path
     uint32_t* err;
 };
@@ -45,6 +46,7 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, const uint16_t
                          const AlignOut& o, cudaStream_t s);
 // uniq list + tile list from an offsets array already on the device.
 // bf16 -> fp16 copy of n elements (n % 8 == 0); out-of-range values set the error word.
+// bf16 rows -> fp16 in the tensor-core operand order (K interleaved in groups of 8)
 cudaError_t launch_bf16_to_f16(const uint16_t* in, uint16_t* out, size_t n, uint32_t* err, cudaStream_t s);
 cudaError_t launch_plan_from_offsets(const int32_t* offsets, int E, int32_t* uniq, Tile* tiles,
                                      DevPlan* plan, cudaStream_t s);

@@ -124,7 +124,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, bool& bad) {
 }
 
 // Copy rows x[sorted[i] / k] -> x_perm[i] for i in [i0, i1), 16 bytes per lane,
-// converting bf16 to fp16 when TO_F16.
+// converting bf16 to fp16 when TO_F16 (then in the tensor-core operand order:
+// K interleaved in groups of 8, see k8_interleave).
 template <bool TO_F16>
 __device__ void gather_rows(const uint16_t* __restrict__ x, int d, int k, const int32_t* __restrict__ sorted,
                             int i0, int i1, uint16_t* __restrict__ x_perm, int warp, int nwarps, uint32_t* err) {
@@ -138,12 +139,9 @@ __device__ void gather_rows(const uint16_t* __restrict__ x, int d, int k, const 
         uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)i * d);
         for (int v = lane; v < vec; v += 32) {
             uint4 q = src[v];
-            if (TO_F16) {
-                q.x = bf16x2_to_f16x2(q.x, bad);
-                q.y = bf16x2_to_f16x2(q.y, bad);
-                q.z = bf16x2_to_f16x2(q.z, bad);
-                q.w = bf16x2_to_f16x2(q.w, bad);
-            }
+            if (TO_F16)
+                q = k8_interleave(bf16x2_to_f16x2(q.x, bad), bf16x2_to_f16x2(q.y, bad), bf16x2_to_f16x2(q.z, bad),
+                                  bf16x2_to_f16x2(q.w, bad));
             dst[v] = q;
         }
     }
@@ -237,12 +235,9 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
                                                           size_t n16, uint32_t* err) {
     bool bad = false;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
-        uint4 q = in[i];
-        q.x = bf16x2_to_f16x2(q.x, bad);
-        q.y = bf16x2_to_f16x2(q.y, bad);
-        q.z = bf16x2_to_f16x2(q.z, bad);
-        q.w = bf16x2_to_f16x2(q.w, bad);
-        out[i] = q;
+        const uint4 q = in[i];
+        out[i] = k8_interleave(bf16x2_to_f16x2(q.x, bad), bf16x2_to_f16x2(q.y, bad), bf16x2_to_f16x2(q.z, bad),
+                               bf16x2_to_f16x2(q.w, bad));
     }
     if (bad) set_error(err, ERRBIT_F16_RANGE);
 }
