@@ -15,15 +15,17 @@
 //   phase 1  gate_up: the CTA takes a contiguous share of the tiles
 //            (touched expert u, 8 features) and computes, for each token routed
 //            to u, the 8 gate and 8 up dot products over d_model, then
-//            h = SiLU(gate) * up (fp16) into a global scratch.
+//            h = SiLU(gate) * up (fp16) into a global scratch.  Inside the CTA
+//            the 8 consumer pairs split the tiles' chunks evenly; a tile cut
+//            between two pairs is finished from their partial sums.
 //   barrier  one grid-wide arrival on a 64-bit counter in the workspace header
 //            (all CTAs are co-resident: one per SM, cooperative launch); the
 //            producer keeps loading phase-2 weights while it is pending.
-//   phase 2  down + combine: the CTA takes a contiguous share of the units
-//            (token t, 16 output features); for each of t's k experts it forms
-//            16 down-projection dot products over d_ff, scales them by the
-//            routing weight, and the unit's k contributions are added in slot
-//            order in fp32 and written to out as bf16.
+//   phase 2  down + combine: the CTA takes a contiguous share of one
+//            token's units (16 output features); for each of the token's k
+//            experts it forms 16 down-projection dot products over d_ff,
+//            scaled by the routing weight; the pairs' partial sums of a unit
+//            are added in pair order in fp32 and written to out as bf16.
 //
 // Inner loop.  One warp holds the A fragment of an m16n8k16 MMA (16 weight
 // rows x 16 codes) in registers, dequantised straight from the packed words:
@@ -38,17 +40,14 @@
 //     C1 = 1024 * sum(x over even k) + 64 * sum(x over odd k),   C2 = sum(x),
 // with C1 and C2 computed once per (token, group) from the same fp16 values.
 //
-// Pipeline.  Warps 16..19 are producers.  Lane 0 of warp 16 takes every chunk
-// in order: it waits until the chunk's ring slot is empty, issues 3D TMA boxes
-// of the packed codes (16 rows x 4 lines of 128 B = 2 groups each, 128-byte
-// swizzle) and marks the slot issued.  Warps 17..19 (chunk q to warp
-// 17 + q % 3, since copying a chunk's scales keeps a warp busy for several
-// hundred cycles) wait for that mark and copy the matching fp16 scales and
-// zeros with 4-byte cp.async; TMA bytes and copies complete the chunk's full
-// mbarrier.  Warps 0..15 form 8 pairs; a tile belongs to one pair
-// and each warp of the pair takes half of every chunk's groups (the slot is
-// released after the warp's last copy from it); the two halves are added
-// through shared memory.
+// Pipeline.  Four independent pipelines: producer warp 16 + i owns a quarter
+// of the ring's slots and feeds consumer pairs 2i and 2i + 1, in chunk order.
+// A chunk is 16 weight rows x 4 lines of 128 B (2 groups each; one TMA box,
+// 128-byte swizzle) plus the rows' fp16 scales and zeros (TMA boxes, plain
+// bulk copies or 4-byte cp.async, by shape), all completing the chunk's full
+// mbarrier.  Warps 0..15 form 8 pairs; each warp of a pair copies its half
+// of a chunk's groups into registers, releases the slot, then computes; the
+// two halves are added through shared memory.
 // Every wait is bounded (2 s), after which the kernel records a timeout in the
 // workspace error word, raises the CTA's abort flag and winds down.
 #include <cfloat>
