@@ -478,6 +478,13 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         for (int i = lane; i < 2 * E; i += 32) cnt_a[i] = 0;
         emask[lane] = 0;
     }
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream (when the driver accepts it), the CTA may start while that kernel
+    // drains: everything above touches only this CTA's shared memory; from
+    // here on global memory (inputs, workspace, outputs) is read and written,
+    // so wait until the previous grid has completed and its writes are
+    // visible.  (Without a programmatic dependency this returns at once.)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (warp < T) {
         // this token's logits into shared memory, then top-k
         float* lrow = lgs + warp * E;
@@ -948,6 +955,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     }
     bar_sync(1, CONSUMER_THREADS);
 
+    // this CTA is in its last phase: the next kernel may be scheduled
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // stage token tok's k rows of h (slot j at row j) and their C1/C2 (the
     // C1/C2 row k is zero); clear the per-(unit, pair) partials
     const int zrow = k;
@@ -1185,12 +1195,25 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = l.smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // cooperative (the grid barrier needs every CTA resident) and, where the
+    // driver accepts it, a programmatic dependent of the previous kernel on the
+    // stream (the kernel waits for it before touching global memory)
+    static int pdl_ok = 1;
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_ok ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, m13, m2, m13s, m13z, m2s, m2z, p);
+    if (e != cudaSuccess && pdl_ok) {
+        // not accepted together with the cooperative launch: plain launch
+        (void)cudaGetLastError();
+        pdl_ok = 0;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, m13, m2, m13s, m13z, m2s, m2z, p);
+    }
     note_launch();
     return e;
 }

@@ -372,3 +372,51 @@ def test_fused_decode_repeated_calls_share_the_grid_barrier(M):
     assert arrivals == 5 * n_sm
     for a, b in ((0, 2), (0, 4), (1, 3)):
         assert torch.equal(outs[a].view(torch.int16), outs[b].view(torch.int16))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["decode", "large_decode"])
+def test_fused_decode_back_to_back_calls_on_one_workspace(M, name):
+    """Consecutive one-kernel decode calls overlap their launches (each waits
+    for the previous kernel before it touches global memory) and share one
+    workspace, whose h rows and grid-barrier counter every call rewrites.  A
+    stream of calls over alternating layers, eager and replayed as a CUDA
+    graph, must give bit-for-bit the outputs of the same calls made one at a
+    time with a synchronisation between them, and report no device error."""
+    import torch
+    cfg = S.CONFIGS[name]
+    nl = 3 if name == "decode" else 2
+    layers = [M.Layer.from_numpy(_layer(cfg, l)) for l in range(nl)]
+    xs = [x_to_dev(S.activations(cfg, l)) for l in range(nl)]
+    lgs = [f32_to_dev(S.router_logits(cfg, l)) for l in range(nl)]
+    ws = M.workspace(max(M.layer_workspace_size(ly, cfg.T, cfg.k) for ly in layers))
+    calls = [M.LayerCall(ly, cfg.T, cfg.k, ws=ws) for ly in layers]
+    ref = []
+    for l in range(nl):
+        o = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+        calls[l](xs[l], lgs[l], o)
+        torch.cuda.synchronize()
+        ref.append(o)
+    seq = [i % nl for i in range(24)]
+    outs = [torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda") for _ in seq]
+    for o, l in zip(outs, seq):
+        calls[l](xs[l], lgs[l], o)
+    torch.cuda.synchronize()
+    assert M.get_device_error(ws) == 0
+    for o, l in zip(outs, seq):
+        assert torch.equal(o.view(torch.int16), ref[l].view(torch.int16))
+    # the same stream of calls captured once and replayed twice
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    for o in outs:
+        o.zero_()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for o, l in zip(outs, seq):
+                calls[l](xs[l], lgs[l], o, stream=s)
+        g.replay()
+        g.replay()
+    s.synchronize()
+    assert M.get_device_error(ws) == 0
+    for o, l in zip(outs, seq):
+        assert torch.equal(o.view(torch.int16), ref[l].view(torch.int16))
