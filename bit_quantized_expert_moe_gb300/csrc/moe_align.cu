@@ -91,15 +91,16 @@ __device__ void emit_plan(int cnt, int e, int E, int32_t* counts, int32_t* offse
 }
 
 // Stable placement of assignments [a0, a1) by one warp, walking them in
-// ascending order 32 at a time.  run[e] holds the next free position of e.
-__device__ void warp_stable_scatter(const int32_t* __restrict__ ids, int a0, int a1, int E, int* run,
+// ascending order 32 at a time.  The id of assignment a is ids[a - ibase];
+// run[e] holds the next free position of e.
+__device__ void warp_stable_scatter(const int32_t* __restrict__ ids, int ibase, int a0, int a1, int E, int* run,
                                     int32_t* __restrict__ sorted, int32_t* __restrict__ inv,
                                     uint32_t* err) {
     const int lane = threadIdx.x & 31;
     const uint32_t lt = (1u << lane) - 1u;
     for (int base = a0; base < a1; base += 32) {
         const int a = base + lane;
-        int e = (a < a1) ? ids[a] : -1;
+        int e = (a < a1) ? ids[a - ibase] : -1;
         const bool valid = (a < a1) && e >= 0 && e < E;
         if (a < a1 && !valid) set_error(err, ERRBIT_RANGE);
         const int key = valid ? e : -1;
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) align_small_kernel(const int32_t
     emit_plan(tid < E ? cnt[tid] : 0, tid, E, o.counts, o.offsets, o.uniq, o.tiles, o.plan, &my_off);
     if (tid < E) run[tid] = my_off;
     __syncthreads();
-    if (tid < 32) warp_stable_scatter(ids, 0, R, E, run, o.sorted, o.inv, o.err);
+    if (tid < 32) warp_stable_scatter(ids, 0, 0, R, E, run, o.sorted, o.inv, o.err);
     if (o.x_perm) {
         __syncthreads();
         gather_any(o, x, d, k, R, tid >> 5, SCAN_THREADS / 32);
@@ -199,15 +200,23 @@ __global__ void __launch_bounds__(256) align_hist_kernel(const int32_t* __restri
 }
 
 // Turns blockcnt[b][e] into the first position of block b's assignments to e.
+// Thread e walks the blocks in batches whose loads are all issued before any
+// store, so the batch costs one memory latency rather than one per block.
 __global__ void __launch_bounds__(SCAN_THREADS) align_scan_kernel(int nblocks, int E, int32_t* __restrict__ blockcnt,
                                                                   AlignOut o) {
+    constexpr int BATCH = 16;
     const int e = threadIdx.x;
     int total = 0;
     if (e < E) {
-        for (int b = 0; b < nblocks; ++b) {
-            const int c = blockcnt[(size_t)b * E + e];
-            blockcnt[(size_t)b * E + e] = total;
-            total += c;
+        for (int b0 = 0; b0 < nblocks; b0 += BATCH) {
+            int c[BATCH];
+#pragma unroll
+            for (int i = 0; i < BATCH; ++i) c[i] = b0 + i < nblocks ? blockcnt[(size_t)(b0 + i) * E + e] : 0;
+#pragma unroll
+            for (int i = 0; i < BATCH; ++i) {
+                if (b0 + i < nblocks) blockcnt[(size_t)(b0 + i) * E + e] = total;
+                total += c[i];
+            }
         }
     }
     int off = 0;
@@ -216,14 +225,18 @@ __global__ void __launch_bounds__(SCAN_THREADS) align_scan_kernel(int nblocks, i
         for (int b = 0; b < nblocks; ++b) blockcnt[(size_t)b * E + e] += off;
 }
 
+// One warp per block of assignments: the block's ids are first copied to
+// shared memory with all loads in flight at once, then placed in order.
 __global__ void __launch_bounds__(32) align_scatter_kernel(const int32_t* __restrict__ ids, int R, int E,
                                                            const int32_t* __restrict__ blockcnt, AlignOut o) {
     __shared__ int run[1024];
-    for (int e = threadIdx.x; e < E; e += 32) run[e] = blockcnt[(size_t)blockIdx.x * E + e];
-    __syncwarp();
+    __shared__ int32_t bid[ALIGN_BLOCK_ROWS];
     const int a0 = blockIdx.x * ALIGN_BLOCK_ROWS;
     const int a1 = min(R, a0 + ALIGN_BLOCK_ROWS);
-    warp_stable_scatter(ids, a0, a1, E, run, o.sorted, o.inv, o.err);
+    for (int e = threadIdx.x; e < E; e += 32) run[e] = blockcnt[(size_t)blockIdx.x * E + e];
+    for (int a = a0 + threadIdx.x; a < a1; a += 32) bid[a - a0] = ids[a];
+    __syncwarp();
+    warp_stable_scatter(bid, a0, a0, a1, E, run, o.sorted, o.inv, o.err);
 }
 
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int d, int k, int R, AlignOut o) {
