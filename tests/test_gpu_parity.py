@@ -328,6 +328,7 @@ def test_decode_layer_kernels_match_oracle(M, decode_kernel, kernel, name):
     (2, 1024, 32, 256, 256, False), # E = 1024, R = 64
     (5, 64, 2, 2048, 1024, True),
     (1, 256, 40, 512, 256, False),  # k > 32: slots j and j + 32 per lane in the router
+    (8, 16, 8, 7168, 2048, False),  # the smallest ring: 8 slots, 2 per producer pipeline
 ])
 def test_fused_decode_layer_shapes(M, T, E, k, d, f, ties):
     import torch
