@@ -45,7 +45,7 @@ constexpr int A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_BYTES = BN * BK * 2;     // 32 KB
 constexpr int P_BYTES = BM * BK / 2;     // 4 KB of packed codes
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + P_BYTES;
-constexpr int B_BOX_ROWS = 32;           // activation rows per TMA box
+constexpr int B_BOX_ROWS = 64;           // activation rows per TMA box (fewer, larger copies: the single producer thread issues every one)
 constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
 constexpr int THREADS = 512;
 constexpr int DQ_WARP0 = 4, DQ_WARPS = 8;
@@ -177,15 +177,18 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 int e, row0, nrows, fb;
                 item_rows<GATEUP>(p, item, e, row0, nrows, fb);
                 const int nbox = ceil_div(nrows, B_BOX_ROWS);
-                const int wrow_a = GATEUP ? e * 2 * p.f + fb * 64 : e * p.d + fb * BM;
-                const int wrow_b = GATEUP ? wrow_a + p.f : wrow_a + 64;
+                const int wrow_a = e * p.d + fb * BM;  // down: first weight row of the block
                 for (int kc = 0; kc < NK; ++kc) {
                     if (!tc::mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     const uint32_t fbar = bar_full + 8 * stage;
                     tc::mbar_arrive_expect_tx(fbar, P_BYTES + nbox * B_BOX_BYTES);
                     const uint32_t dp = sP + stage * P_BYTES;
-                    tc::tma_load_2d(dp, &map_w, fbar, kc * (BK / 8), wrow_a);
-                    tc::tma_load_2d(dp + P_BYTES / 2, &map_w, fbar, kc * (BK / 8), wrow_b);
+                    // the stage's 128 rows of codes in one box: gate_up's 64 gate and
+                    // 64 up rows (3D map over the expert halves), down's 128 rows
+                    if (GATEUP)
+                        tc::tma_load_3d(dp, &map_w, fbar, kc * (BK / 8), fb * 64, 2 * e);
+                    else
+                        tc::tma_load_2d(dp, &map_w, fbar, kc * (BK / 8), wrow_a);
                     const uint32_t db = sB + stage * B_BYTES;
                     for (int b = 0; b < nbox; ++b)
                         tc::tma_load_2d(db + b * B_BOX_BYTES, &map_x, fbar, kc * BK, row0 + b * B_BOX_ROWS);
@@ -457,9 +460,21 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
 
     const uint64_t rows_w = (uint64_t)E * (GATEUP ? 2 * (uint64_t)f : (uint64_t)d);
     CUtensorMap map_w, map_x;
-    if (!make_map(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, GATEUP ? in.w13_q : in.w2_q, (uint64_t)p.K / 8,
-                  rows_w, BK / 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (GATEUP) {
+        // codes as [expert * 2 + (gate, up)][feature][K / 8 words]: box = 8 words
+        // of 64 features of both halves
+        EncodeFn enc = get_encode();
+        const cuuint64_t dims[3] = {(cuuint64_t)p.K / 8, (cuuint64_t)f, (cuuint64_t)E * 2};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.K / 2, (cuuint64_t)f * p.K / 2};
+        const cuuint32_t box[3] = {BK / 8, 64, 2}, estr[3] = {1, 1, 1};
+        if (!enc || enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(in.w13_q), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else if (!make_map(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, in.w2_q, (uint64_t)p.K / 8, rows_w, BK / 8, BM,
+                         CU_TENSOR_MAP_SWIZZLE_NONE)) {
         return cudaErrorInvalidValue;
+    }
     if (!make_map(&map_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, GATEUP ? in.x16 : in.h16, (uint64_t)p.K,
                   (uint64_t)R, BK, B_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
