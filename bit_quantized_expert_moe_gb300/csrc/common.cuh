@@ -122,10 +122,6 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     return *reinterpret_cast<float2*>(&rd);
 }
 
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
-    return __uint_as_float(((uint32_t)b) << 16);
-}
-
 __device__ __forceinline__ float half_bits_to_float(uint16_t b) {
     return __half2float(__ushort_as_half(b));
 }

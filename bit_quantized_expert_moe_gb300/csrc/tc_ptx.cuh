@@ -131,11 +131,6 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
-// Arrive on `bar` once every cp.async issued so far by this thread has landed
-// (the arrival is not pre-counted: the barrier's expected count includes it).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
-}
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (tensor core).
 __device__ __forceinline__ void fence_proxy_async_smem() {
