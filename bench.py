@@ -59,6 +59,18 @@ def dist_env():
     return rank, world, local
 
 
+def job_rate(torch, ms_local, tokens_per_rank_step, world, device):
+    """Whole-job throughput of `world` replicas: the step time is the slowest
+    rank's (max over ranks), the tokens are every rank's.  Returns (tokens/s,
+    max ms per step)."""
+    ms = float(ms_local)
+    if world > 1:
+        tt = torch.tensor([ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    return tokens_per_rank_step * world / (ms / 1e3), ms
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -234,13 +246,8 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-    ms = t0.elapsed_time(t1) / steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    value, ms = job_rate(torch, t0.elapsed_time(t1) / steps, wl.tokens_per_step(), world, dev)
     tokens = wl.tokens_per_step() * world
-    value = tokens / (ms / 1e3)
 
     # -------------------------------------- stage events of the same step (graph)
     prof = M.StageProfiler(wl.L)
@@ -349,12 +356,8 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
                 e2e_step()
             a1.record(s)
             s.synchronize()
-        ems = a0.elapsed_time(a1) / steps
-        if world > 1:
-            tt = torch.tensor([ems], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            ems = float(tt.item())
-        e2e = {"value": round(tokens / (ems / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        e2e_value, ems = job_rate(torch, a0.elapsed_time(a1) / steps, wl.tokens_per_step(), world, dev)
+        e2e = {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ems, 4),
                "path": "pinned host x/logits -> device, graph replay of moe_layer_forward x L, out -> pinned host"}
 
