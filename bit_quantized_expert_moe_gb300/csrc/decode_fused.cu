@@ -62,12 +62,21 @@ namespace {
 
 using tc::WAIT_LIMIT_NS;
 
-constexpr int CW = 16;                          // consumer warps (8 pairs)
-constexpr int NPAIR = CW / 2;
-constexpr int NQ = 4;                           // pipelines: producer warp 16 + i feeds pairs 2i and 2i + 1
-constexpr int PRODUCER_WARP = CW;               // first producer warp
-constexpr int NTHREADS = 32 * (CW + NQ);
-constexpr int CONSUMER_THREADS = 32 * CW;
+// Warp layout of one instantiation: NQ producer pipelines (producer warp
+// CW + i feeds consumer pairs 2i and 2i + 1), 2 NQ pairs, 4 NQ consumer warps.
+// Small layers take NQ = 3 (12 consumer warps: 128 registers each instead of
+// 96, and fewer warps sharing a sub-partition when every pair computes at
+// once); layers with megabytes of weights per CTA take NQ = 4 (more math in
+// flight).
+template <int NQ_>
+struct Shape {
+    static constexpr int NQ = NQ_;
+    static constexpr int NPAIR = 2 * NQ_;
+    static constexpr int CW = 2 * NPAIR;
+    static constexpr int PRODUCER_WARP = CW;
+    static constexpr int NTHREADS = 32 * (CW + NQ_);
+    static constexpr int CONSUMER_THREADS = 32 * CW;
+};
 constexpr int LINES = 4;                        // 128-byte lines (2 groups each) per chunk row
 constexpr int CHUNK_GROUPS = 2 * LINES;         // groups of 128 codes per chunk
 constexpr int BOX_BYTES = 8 * LINES * 128;      // 8 rows x 4 lines (rows g; rows g + 8 follow)
@@ -115,7 +124,7 @@ struct Params {
     uint32_t* err;
     unsigned long long* bar_count;  // grid-barrier arrivals (only grows)
     int T, k, E, d, f;
-    int nslot;                 // a multiple of NQ: pipeline i owns slots [i * nslot / NQ, (i + 1) * nslot / NQ)
+    int nslot;                 // a multiple of the pipeline count NQ: pipeline i owns slots [i, i + 1) * nslot / NQ
     uint32_t off_sz, off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab;
     uint32_t off_cnt;          // phase-0 counters inside the ring, after the logits
     int xb_stride, hs_stride;  // bytes per staged row
@@ -429,11 +438,15 @@ __device__ __forceinline__ void consume_chunk(float (&acc)[4], uint32_t full, ui
 }
 
 // ------------------------------------------------------------------ kernel
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int NQ_>
+__global__ void __launch_bounds__(Shape<NQ_>::NTHREADS, 1)
 decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_constant__ CUtensorMap map2,
                     const __grid_constant__ CUtensorMap map13s, const __grid_constant__ CUtensorMap map13z,
                     const __grid_constant__ CUtensorMap map2s, const __grid_constant__ CUtensorMap map2z,
                     const Params p) {
+    constexpr int NQ = Shape<NQ_>::NQ, NPAIR = Shape<NQ_>::NPAIR, CW = Shape<NQ_>::CW;
+    constexpr int PRODUCER_WARP = Shape<NQ_>::PRODUCER_WARP, NTHREADS = Shape<NQ_>::NTHREADS;
+    constexpr int CONSUMER_THREADS = Shape<NQ_>::CONSUMER_THREADS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sbase = smem_u32(sm);
@@ -1034,7 +1047,8 @@ struct Layout {
     int xb_stride, hs_stride;
 };
 
-bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
+bool plan_layout(int T, int k, int E, int d, int f, int G, int nq, Layout* L) {
+    const int NQ = nq, NPAIR = 2 * nq;
     if (T < 1 || T > MAX_T || k < 1 || T * k > MAX_R || E < 1 || E > 1024 || G < T) return false;
     if (d % 256 || f % 256 || f >= 65536) return false;  // (a feature index is packed in 16 bits)
     Layout l{};
@@ -1095,17 +1109,27 @@ bool plan_layout(int T, int k, int E, int d, int f, int G, Layout* L) {
 
 }  // namespace
 
+// Pipelines for a layer: 3 while the routed weights per CTA are small (at most
+// T k experts touched), else 4 (both measured on the BASELINE-shaped layers:
+// 12 consumer warps win at d_model 2048, 16 at d_model 7168).
+int pick_nq(int T, int k, int E, int d, int f, int G) {
+    const double bytes = (double)std::min(T * k, E) * 3.0 * d * f * 0.53125 / G;
+    return bytes <= 1.0e6 ? 3 : 4;
+}
+
 bool decode_fused_supported(int T, int k, int E, int d, int f) {
     Layout l;
-    return plan_layout(T, k, E, d, f, num_sms(), &l);
+    const int G = num_sms();
+    return plan_layout(T, k, E, d, f, G, pick_nq(T, k, E, d, f, G), &l);
 }
 
 cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     const moe_w4_layer& W = *in.L;
     const int E = W.E, d = W.d_model, f = W.d_ff;
     const int G = num_sms();
+    const int nq = pick_nq(in.T, in.k, E, d, f, G);
     Layout l;
-    if (!plan_layout(in.T, in.k, E, d, f, G, &l)) return cudaErrorInvalidValue;
+    if (!plan_layout(in.T, in.k, E, d, f, G, nq, &l)) return cudaErrorInvalidValue;
     // codes as 32-word lines: gate_up [expert * 2 + (gate, up)][feature][line][32
     // words], box 8 features of both halves; down [row][line][32 words], box 16 rows
     CUtensorMap m13, m2;
@@ -1178,21 +1202,23 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     p.fd_nch2 = make_fastdiv((uint32_t)ceil_div(f / 128, CHUNK_GROUPS));
     p.fd_nfb1 = make_fastdiv((uint32_t)(f / 8));
     p.fd_k = make_fastdiv((uint32_t)in.k);
-    p.fd_ns4 = make_fastdiv((uint32_t)(l.nslot / NQ));
+    p.fd_ns4 = make_fastdiv((uint32_t)(l.nslot / nq));
     p.fd_xw = make_fastdiv((uint32_t)(d / 8));
     p.fd_hw = make_fastdiv((uint32_t)(f / 8));
     p.sz2_rs = p.sz2_mode == SZ_BULK ? (int)Gf * 2 : 16;
 
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_LIMIT);
+    static bool configured[2] = {false, false};
+    if (!configured[nq - 3]) {
+        cudaError_t e = nq == 3 ? cudaFuncSetAttribute(decode_fused_kernel<3>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT)
+                                : cudaFuncSetAttribute(decode_fused_kernel<4>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_LIMIT);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured[nq - 3] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
-    cfg.blockDim = dim3(NTHREADS);
+    cfg.blockDim = dim3(nq == 3 ? Shape<3>::NTHREADS : Shape<4>::NTHREADS);
     cfg.dynamicSmemBytes = l.smem;
     cfg.stream = s;
     // cooperative (the grid barrier needs every CTA resident) and, where the
@@ -1206,13 +1232,17 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_ok ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, m13, m2, m13s, m13z, m2s, m2z, p);
+    auto launch = [&]() {
+        return nq == 3 ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<3>, m13, m2, m13s, m13z, m2s, m2z, p)
+                       : cudaLaunchKernelEx(&cfg, decode_fused_kernel<4>, m13, m2, m13s, m13z, m2s, m2z, p);
+    };
+    cudaError_t e = launch();
     if (e != cudaSuccess && pdl_ok) {
         // not accepted together with the cooperative launch: plain launch
         (void)cudaGetLastError();
         pdl_ok = 0;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, decode_fused_kernel, m13, m2, m13s, m13z, m2s, m2z, p);
+        e = launch();
     }
     note_launch();
     return e;
