@@ -40,14 +40,14 @@
 //     C1 = 1024 * sum(x over even k) + 64 * sum(x over odd k),   C2 = sum(x),
 // with C1 and C2 computed once per (token, group) from the same fp16 values.
 //
-// Pipeline.  Four independent pipelines: producer warp 16 + i owns a quarter
-// of the ring's slots and feeds consumer pairs 2i and 2i + 1, in chunk order.
-// A chunk is 16 weight rows x 4 lines of 128 B (2 groups each; one TMA box,
-// 128-byte swizzle) plus the rows' fp16 scales and zeros (TMA boxes, plain
-// bulk copies or 4-byte cp.async, by shape), all completing the chunk's full
-// mbarrier.  Warps 0..15 form 8 pairs; each warp of a pair copies its half
-// of a chunk's groups into registers, releases the slot, then computes; the
-// two halves are added through shared memory.
+// Pipeline.  NQ independent pipelines (3 or 4, see Shape): producer warp
+// CW + i owns 1/NQ of the ring's slots and feeds consumer pairs 2i and 2i + 1,
+// in chunk order.  A chunk is 16 weight rows x 4 lines of 128 B (2 groups
+// each; one TMA box, 128-byte swizzle) plus the rows' fp16 scales and zeros
+// (TMA boxes, plain bulk copies or 4-byte cp.async, by shape), all completing
+// the chunk's full mbarrier.  Consumer warps 0 .. CW - 1 form pairs; each warp
+// of a pair copies its half of a chunk's groups into registers, releases the
+// slot, then computes; the two halves are added through shared memory.
 // Every wait is bounded (2 s), after which the kernel records a timeout in the
 // workspace error word, raises the CTA's abort flag and winds down.
 #include <cfloat>
