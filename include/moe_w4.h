@@ -212,7 +212,11 @@ moe_status_t moe_combine(const void* y_perm_bf16, const int32_t* inv, const floa
  * The whole layer: stages 1-4 on one stream, nothing allocated, no host sync.
  * With T <= 8 and T*k <= 64 the layer runs as ONE kernel (routing repeated in
  * every CTA, gate_up, one grid barrier, down with the combine fused; one CTA
- * per SM, cooperative launch).  Its intermediate precision: activations and h
+ * per SM, cooperative launch).  Consecutive calls on a stream may be launched
+ * as programmatic dependents of the previous kernel: a call's CTAs start their
+ * shared-memory setup early but touch no global memory (inputs, outputs,
+ * workspace) before the previous kernel on the stream has completed, so stream
+ * order is unchanged.  Its intermediate precision: activations and h
  * in fp16 (|x|, |h| < 65504, else MOE_ERR_F16_RANGE), products of the exact
  * int4 codes with fp32 accumulation, zero and scale applied per group of 128
  * in fp32.  MOE_W4_DECODE_KERNEL=split runs the stage chain instead.
