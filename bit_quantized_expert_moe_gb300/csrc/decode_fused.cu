@@ -46,8 +46,9 @@
 // each; one TMA box, 128-byte swizzle) plus the rows' fp16 scales and zeros
 // (TMA boxes, plain bulk copies or 4-byte cp.async, by shape), all completing
 // the chunk's full mbarrier.  Consumer warps 0 .. CW - 1 form pairs; each warp
-// of a pair copies its half of a chunk's groups into registers, releases the
-// slot, then computes; the two halves are added through shared memory.
+// of a pair takes half of a chunk's groups, loading each group's codes into
+// registers right before its math and releasing the slot after the last
+// group's loads; the two halves are added through shared memory.
 // Every wait is bounded (2 s), after which the kernel records a timeout in the
 // workspace error word, raises the CTA's abort flag and winds down.
 #include <cfloat>
@@ -364,20 +365,14 @@ __device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ush
 __device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
 
 // This warp's NG groups (gb .. gb + NG - 1 of the chunk whose codes are at sa
-// and whose scales and zeros are at szs): all of
-// their codes, scales and zeros are copied into registers first and the slot
-// is given back before any math, so a slot is held only for the copy.
+// and whose scales and zeros are at szs): the scales and zeros are copied
+// into registers first, then each group's codes are loaded right before its
+// math (the next group's loads overlap the current group's MMAs); the slot is
+// given back after the last group's loads.
 template <int NG>
 __device__ __forceinline__ void consume_groups(float (&acc)[4], uint32_t sa, uint32_t szs, uint32_t rs, uint32_t empty,
                                                int gb, int g, int t, int gi0, uint32_t brow_a, uint32_t bact,
                                                uint32_t c0_a, uint32_t c1_a, float wscale) {
-    uint4 wa[NG], wb[NG];
-#pragma unroll
-    for (int i = 0; i < NG; ++i) {
-        const uint32_t aoff = a_offset(gb + i, g, t);
-        wa[i] = lds128(sa + aoff);
-        wb[i] = lds128(sa + BOX_BYTES + aoff);
-    }
     // scales and zeros kept as fp16 pairs until use: sz[0..3] = s0, z0, s1, z1
     // (rows g and g + 8), word w holds groups 2w and 2w + 1 of this warp's NG
     constexpr int NW = (NG + 1) / 2;
@@ -403,15 +398,19 @@ __device__ __forceinline__ void consume_groups(float (&acc)[4], uint32_t sa, uin
                 sz[a][w] = lo | (hi << 16);
             }
     }
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty);
 #pragma unroll
     for (int i = 0; i < NG; ++i) {
+        const uint32_t aoff = a_offset(gb + i, g, t);
+        const uint4 wai = lds128(sa + aoff), wbi = lds128(sa + BOX_BYTES + aoff);
+        if (i == NG - 1) {
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty);
+        }
         const uint32_t gi = (uint32_t)(gi0 + gb + i);
         float v[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) v[a] = (i & 1) ? half_hi(sz[a][i >> 1]) : half_lo(sz[a][i >> 1]);
-        compute_group(acc, wa[i], wb[i], v[0] * wscale, v[1], v[2] * wscale, v[3], t, brow_a + 256u * gi, bact,
+        compute_group(acc, wai, wbi, v[0] * wscale, v[1], v[2] * wscale, v[3], t, brow_a + 256u * gi, bact,
                       c0_a + 8u * gi, c1_a + 8u * gi);
     }
 }
