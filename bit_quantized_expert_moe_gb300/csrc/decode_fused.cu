@@ -979,13 +979,36 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     if (!*abort_flag && n2u > 0) {
         const int tid = threadIdx.x;
         const int wpr = f >> 3;  // 16-byte words per row, a multiple of 32
-        for (int wi = tid; wi < k * wpr; wi += CONSUMER_THREADS) {
-            const int lr = (int)fd_div((uint32_t)wi, p.fd_hw), wr = wi - lr * wpr;
-            const uint4 o = ldg_cg16(p.hb + (size_t)tab.pos[tok * k + lr] * (f * 2) + 16 * (size_t)wr);
-            sts128(hs + (uint32_t)(lr * p.hs_stride) + 16u * wr, o);
-            // a staged word holds one word's 8 values in MMA order (staged_offset)
-            const float2 c = halfwarp_sum(word_c1c2(o));
-            if ((lane & 15) == 0) ch[lr * Gf + (wr >> 4)] = c;
+        // h is stored in the staged order already.  The 16-warp instantiation
+        // (over a megabyte of weights per CTA) copies first, all of a thread's
+        // words in flight at once, then sums the words it copied (1.3 us less
+        // per d_model 7168 layer); the 12-warp one loads and sums word by
+        // word, which measured faster there (the copy form left its staging
+        // time unchanged and slowed its phase loops by ~0.5 us per layer).
+        if constexpr (NQ_ == 4) {
+            const int nw = k * wpr;
+            for (int wi = tid; wi < nw; wi += CONSUMER_THREADS) {
+                const int lr = (int)fd_div((uint32_t)wi, p.fd_hw), wr = wi - lr * wpr;
+                cp_async16(hs + (uint32_t)(lr * p.hs_stride) + 16u * wr,
+                           p.hb + (size_t)tab.pos[tok * k + lr] * (f * 2) + 16 * (size_t)wr);
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            for (int wi = tid; wi < nw; wi += CONSUMER_THREADS) {
+                const int lr = (int)fd_div((uint32_t)wi, p.fd_hw), wr = wi - lr * wpr;
+                const uint4 o = lds128(hs + (uint32_t)(lr * p.hs_stride) + 16u * wr);
+                // a staged word holds one word's 8 values in MMA order (staged_offset)
+                const float2 c = halfwarp_sum(word_c1c2(o));
+                if ((lane & 15) == 0) ch[lr * Gf + (wr >> 4)] = c;
+            }
+        } else {
+            for (int wi = tid; wi < k * wpr; wi += CONSUMER_THREADS) {
+                const int lr = (int)fd_div((uint32_t)wi, p.fd_hw), wr = wi - lr * wpr;
+                const uint4 o = ldg_cg16(p.hb + (size_t)tab.pos[tok * k + lr] * (f * 2) + 16 * (size_t)wr);
+                sts128(hs + (uint32_t)(lr * p.hs_stride) + 16u * wr, o);
+                // a staged word holds one word's 8 values in MMA order (staged_offset)
+                const float2 c = halfwarp_sum(word_c1c2(o));
+                if ((lane & 15) == 0) ch[lr * Gf + (wr >> 4)] = c;
+            }
         }
         for (int i = tid; i < Gf; i += CONSUMER_THREADS) ch[zrow * Gf + i] = make_float2(0.f, 0.f);
         for (int i = tid; i < n2u * NPAIR * 16; i += CONSUMER_THREADS) red2[i] = 0.f;
