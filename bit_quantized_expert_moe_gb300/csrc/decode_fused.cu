@@ -486,9 +486,11 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
                 tc::tma_prefetch_desc(&map2z);
             }
         }
-    } else if (warp == PRODUCER_WARP + 1) {
+    } else if (warp == 0) {
+        // the sort's counters (warp 0 sorts right after routing, see below)
         for (int i = lane; i < 2 * E; i += 32) cnt_a[i] = 0;
         emask[lane] = 0;
+        __syncwarp();
     }
     // Launched as a programmatic dependent of the previous kernel on the
     // stream (when the driver accepts it), the CTA may start while that kernel
@@ -504,6 +506,80 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
         for (int e = lane; e < E; e += 32) lrow[e] = __ldg(src + e);
         __syncwarp();
         route_token(lrow, E, k, &tab.ids[warp * k], &tab.w[warp * k]);
+        // every token routed: warp 0 sorts while the other warps still stage
+        // the activations
+        bar_sync(15, 32 * T);
+        if (warp == 0) {
+            // stable counting sort of the R <= 64 assignments by expert: per-expert
+            // counts of the two halves, the touched-expert bitmask (ascending expert
+            // list by a warp scan), ranks inside an expert from __match_any_sync
+            const int a0 = lane, a1 = lane + 32;
+            const bool v0 = a0 < R, v1 = a1 < R;
+            const int e0 = v0 ? tab.ids[a0] : 0, e1 = v1 ? tab.ids[a1] : 0;
+            if (v0) {
+                atomicAdd(&cnt_a[e0], 1);
+                atomicOr(&emask[e0 >> 5], 1u << (e0 & 31));
+            }
+            if (v1) {
+                atomicAdd(&cnt_b[e1], 1);
+                atomicOr(&emask[e1 >> 5], 1u << (e1 & 31));
+            }
+            const uint32_t m0 = __match_any_sync(0xffffffffu, v0 ? e0 : -1 - lane);
+            const uint32_t m1 = __match_any_sync(0xffffffffu, v1 ? e1 : -1 - lane);
+            const uint32_t lt = (1u << lane) - 1u;
+            __syncwarp();
+            // ascending expert list: lane l owns bitmask word l
+            const uint32_t w = emask[lane];
+            int incl = __popc(w);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int U = __shfl_sync(0xffffffffu, incl, 31);
+            int pre = incl - __popc(w);
+            wpre[lane] = pre;
+            for (uint32_t b = w; b; b &= b - 1) tab.uexp[pre++] = 32 * lane + (__ffs(b) - 1);
+            __syncwarp();
+            // expert counts and offsets in list order (U <= 64)
+            const int c0 = lane < U ? cnt_a[tab.uexp[lane]] + cnt_b[tab.uexp[lane]] : 0;
+            const int c1 = lane + 32 < U ? cnt_a[tab.uexp[lane + 32]] + cnt_b[tab.uexp[lane + 32]] : 0;
+            int s0 = c0, s1 = c1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y0 = __shfl_up_sync(0xffffffffu, s0, o);
+                const int y1 = __shfl_up_sync(0xffffffffu, s1, o);
+                if (lane >= o) {
+                    s0 += y0;
+                    s1 += y1;
+                }
+            }
+            const int tot0 = __shfl_sync(0xffffffffu, s0, 31);
+            if (lane < U) {
+                tab.ucnt[lane] = c0;
+                tab.uoff[lane] = s0 - c0;
+            }
+            if (lane + 32 < U) {
+                tab.ucnt[lane + 32] = c1;
+                tab.uoff[lane + 32] = tot0 + s1 - c1;
+            }
+            __syncwarp();
+            // permuted position of each assignment
+            auto uidx = [&](int e) {
+                return wpre[e >> 5] + __popc(emask[e >> 5] & ((1u << (e & 31)) - 1u));
+            };
+            if (v0) {
+                const int pos = tab.uoff[uidx(e0)] + __popc(m0 & lt);
+                tab.pos[a0] = pos;
+                tab.ptok[pos] = (int)fd_div((uint32_t)a0, p.fd_k);
+            }
+            if (v1) {
+                const int pos = tab.uoff[uidx(e1)] + cnt_a[e1] + __popc(m1 & lt);
+                tab.pos[a1] = pos;
+                tab.ptok[pos] = (int)fd_div((uint32_t)a1, p.fd_k);
+            }
+            if (lane == 0) tab.n_uniq = U;
+        }
     } else if (warp < CW) {
         // activations -> fp16 in MMA order, plus C1/C2 per (token, group); the
         // C1/C2 row T is zero (B columns without a token)
@@ -528,78 +604,6 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
             if ((lane & 15) == 0) cx[t * Gd + (wr >> 4)] = c;
         }
         for (int i = tid; i < Gd; i += nthr) cx[T * Gd + i] = make_float2(0.f, 0.f);
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // stable counting sort of the R <= 64 assignments by expert: per-expert
-        // counts of the two halves, the touched-expert bitmask (ascending expert
-        // list by a warp scan), ranks inside an expert from __match_any_sync
-        const int a0 = lane, a1 = lane + 32;
-        const bool v0 = a0 < R, v1 = a1 < R;
-        const int e0 = v0 ? tab.ids[a0] : 0, e1 = v1 ? tab.ids[a1] : 0;
-        if (v0) {
-            atomicAdd(&cnt_a[e0], 1);
-            atomicOr(&emask[e0 >> 5], 1u << (e0 & 31));
-        }
-        if (v1) {
-            atomicAdd(&cnt_b[e1], 1);
-            atomicOr(&emask[e1 >> 5], 1u << (e1 & 31));
-        }
-        const uint32_t m0 = __match_any_sync(0xffffffffu, v0 ? e0 : -1 - lane);
-        const uint32_t m1 = __match_any_sync(0xffffffffu, v1 ? e1 : -1 - lane);
-        const uint32_t lt = (1u << lane) - 1u;
-        __syncwarp();
-        // ascending expert list: lane l owns bitmask word l
-        const uint32_t w = emask[lane];
-        int incl = __popc(w);
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const int U = __shfl_sync(0xffffffffu, incl, 31);
-        int pre = incl - __popc(w);
-        wpre[lane] = pre;
-        for (uint32_t b = w; b; b &= b - 1) tab.uexp[pre++] = 32 * lane + (__ffs(b) - 1);
-        __syncwarp();
-        // expert counts and offsets in list order (U <= 64)
-        const int c0 = lane < U ? cnt_a[tab.uexp[lane]] + cnt_b[tab.uexp[lane]] : 0;
-        const int c1 = lane + 32 < U ? cnt_a[tab.uexp[lane + 32]] + cnt_b[tab.uexp[lane + 32]] : 0;
-        int s0 = c0, s1 = c1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y0 = __shfl_up_sync(0xffffffffu, s0, o);
-            const int y1 = __shfl_up_sync(0xffffffffu, s1, o);
-            if (lane >= o) {
-                s0 += y0;
-                s1 += y1;
-            }
-        }
-        const int tot0 = __shfl_sync(0xffffffffu, s0, 31);
-        if (lane < U) {
-            tab.ucnt[lane] = c0;
-            tab.uoff[lane] = s0 - c0;
-        }
-        if (lane + 32 < U) {
-            tab.ucnt[lane + 32] = c1;
-            tab.uoff[lane + 32] = tot0 + s1 - c1;
-        }
-        __syncwarp();
-        // permuted position of each assignment
-        auto uidx = [&](int e) {
-            return wpre[e >> 5] + __popc(emask[e >> 5] & ((1u << (e & 31)) - 1u));
-        };
-        if (v0) {
-            const int pos = tab.uoff[uidx(e0)] + __popc(m0 & lt);
-            tab.pos[a0] = pos;
-            tab.ptok[pos] = (int)fd_div((uint32_t)a0, p.fd_k);
-        }
-        if (v1) {
-            const int pos = tab.uoff[uidx(e1)] + cnt_a[e1] + __popc(m1 & lt);
-            tab.pos[a1] = pos;
-            tab.ptok[pos] = (int)fd_div((uint32_t)a1, p.fd_k);
-        }
-        if (lane == 0) tab.n_uniq = U;
     }
     __syncthreads();
     if (cta == 0 && p.ids_out)
