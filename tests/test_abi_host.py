@@ -7,6 +7,8 @@ during argument checking, so nothing is ever launched with them.
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -30,7 +32,7 @@ def M():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:moe_status_t|size_t|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:moe_status_t|size_t|uint64_t|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -116,3 +118,53 @@ def test_stage_entry_points_reject_bad_arguments(M):
     assert lib.moe_expert_ffn_w4a16(ctypes.byref(L), P, None, 16, None, P, P, 1 << 30, None) == INVALID
     assert lib.moe_expert_ffn_w4a16(ctypes.byref(L), P + 2, P, 16, None, P, P, 1 << 30, None) == MISALIGNED
     assert lib.moe_get_device_error(None, None) == INVALID
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe_w4.h"
+
+int main(void) {
+    moe_w4_layer L;
+    memset(&L, 0, sizeof L);
+    L.E = 8;
+    L.d_model = 256;
+    L.d_ff = 512;
+    L.group = 128;
+    /* sizes are checked against a complete, aligned layer; nothing is read */
+    L.w13_q = L.w2_q = (const uint32_t*)(uintptr_t)0x100000;
+    L.w13_s = L.w13_z = L.w2_s = L.w2_z = (const uint16_t*)(uintptr_t)0x100000;
+    const size_t ws = moe_layer_workspace_size(&L, 8, 2);
+    /* a null layer is rejected on the host, before anything is launched */
+    const moe_status_t st = moe_layer_forward(NULL, NULL, NULL, 8, 2, NULL, NULL, NULL, 0, NULL);
+    printf("%s|%s|%zu|%d\n", moe_version(), moe_status_str(MOE_OK), ws, (int)st);
+    return (ws > 256 && st == MOE_ERR_INVALID_ARG) ? 0 : 1;
+}
+"""
+
+
+def test_header_compiles_as_c99_and_links(M, tmp_path):
+    """The boundary is usable from plain C: the header compiles as C99 with
+    warnings as errors, a program links against the library, and its host-side
+    calls behave as documented."""
+    gcc = shutil.which("gcc")
+    if gcc is None:  # pragma: no cover
+        pytest.skip("gcc not found")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    cuda_lib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
+    lib_dir = os.path.dirname(M.LIB_PATH)
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+           str(src), M.LIB_PATH, f"-Wl,-rpath,{lib_dir}", f"-Wl,-rpath,{cuda_lib}", f"-Wl,-rpath-link,{cuda_lib}",
+           "-o", str(exe)]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.stdout, r.stderr)
+    version, ok, ws, st = r.stdout.strip().split("|")
+    assert version == M.version() and ok == M.status_str(OK)
+    assert int(ws) == M.lib().moe_layer_workspace_size(ctypes.byref(fake_layer(M)), 8, 2)
+    assert int(st) == INVALID
