@@ -9,6 +9,7 @@ import os
 import re
 import shutil
 import subprocess
+import sys
 
 import pytest
 
@@ -168,3 +169,31 @@ def test_header_compiles_as_c99_and_links(M, tmp_path):
     assert version == M.version() and ok == M.status_str(OK)
     assert int(ws) == M.lib().moe_layer_workspace_size(ctypes.byref(fake_layer(M)), 8, 2)
     assert int(st) == INVALID
+
+
+def test_binding_fails_loudly_without_the_library():
+    """No CPU fallback: without the built library every call raises."""
+    code = ("import bit_quantized_expert_moe_gb300 as M\n"
+            "M.LIB_PATH = '/nonexistent/libmoe_w4.so'\n"
+            "M._lib = None\n"
+            "try:\n"
+            "    M.lib()\n"
+            "    print('loaded')\n"
+            "except RuntimeError as e:\n"
+            "    print('raised', 'no CPU fallback' in str(e))\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "raised True"
+
+
+def test_binding_rejects_host_tensors(M):
+    """Host (CPU) tensors are refused before any library call: the layer runs
+    only on the device."""
+    import torch
+    E, d, f = 8, 256, 512
+    w = lambda *s: torch.zeros(s, dtype=torch.int32)
+    h = lambda *s: torch.zeros(s, dtype=torch.float16)
+    layer = M.Layer(E=E, d_model=d, d_ff=f, w13_q=w(E, 2 * f, d // 8), w13_s=h(E, 2 * f, d // 128),
+                    w13_z=h(E, 2 * f, d // 128), w2_q=w(E, d, f // 8), w2_s=h(E, d, f // 128), w2_z=h(E, d, f // 128))
+    with pytest.raises(ValueError, match="device tensor"):
+        M.LayerCall(layer, 2, 2)
