@@ -396,3 +396,37 @@ def test_planted_transposed_down_and_gate_up_swap(monkeypatch):
 
 def test_planted_dropped_silu(monkeypatch):
     _pins_fail(monkeypatch, "silu", lambda g: g, test_single_expert_is_textbook_mlp)
+
+
+def test_planted_full_softmax_not_renormalised(monkeypatch):
+    # combine weights taken from a softmax over all E logits, not over the k
+    # selected ones
+    real = OM.route_topk
+
+    def bad(logits, k):
+        ids, _ = real(logits, k)
+        lg = np.asarray(logits, np.float64)
+        ex = np.exp(lg - lg.max(1, keepdims=True))
+        full = ex / ex.sum(1, keepdims=True)
+        return ids, np.take_along_axis(full, ids.astype(np.int64), 1)
+    _pins_fail(monkeypatch, "route_topk", bad, test_topk_invariants_and_weights)
+    _pins_fail(monkeypatch, "route_topk", bad, test_topk_golden_examples)
+
+
+def test_planted_combine_slot_weights_reversed(monkeypatch):
+    real = OM.combine
+
+    def bad(y_perm, inv, w, T, k):
+        return real(y_perm, inv, np.ascontiguousarray(w[:, ::-1]), T, k)
+    _pins_fail(monkeypatch, "combine", bad, test_layer_matches_dense_masked_bruteforce)
+
+
+def test_planted_combine_reads_through_sorted(monkeypatch):
+    # rows fetched with the forward permutation instead of its inverse
+    def bad(y_perm, inv, w, T, k):
+        sorted_ = np.argsort(inv)
+        out = np.zeros((T, y_perm.shape[1]))
+        for j in range(k):
+            out += w[:, j:j + 1] * y_perm[sorted_[np.arange(T) * k + j]]
+        return out
+    _pins_fail(monkeypatch, "combine", bad, test_layer_matches_dense_masked_bruteforce)
