@@ -377,10 +377,39 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
 
 
 # --------------------------------------------------------------------------
-def cpu_baseline(wl_name, budget_s=15.0, max_units=None):
-    """The oracle, as it stands, on the host cores: a bounded sample of the workload."""
+def bf16_host_to_f64(t):
+    """bf16 torch tensor on the host -> float64 numpy (exact)."""
+    import torch
+    u = t.contiguous().view(torch.int16).numpy().view(np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def parity_vs_oracle(gpu_out, gpu_ids, oracle_layers):
+    """The step's outputs against the oracle's, per layer: max|err| / rms(ref)
+    and mean|err| / mean|ref| (the worst layer of each), and whether the
+    routing ids match exactly."""
+    worst_max, worst_mean, ids_exact = 0.0, 0.0, True
+    for l, ref, ids in oracle_layers:
+        got = bf16_host_to_f64(gpu_out[l])
+        err = np.abs(got - ref)
+        rms = float(np.sqrt(np.mean(ref * ref)))
+        worst_max = max(worst_max, float(err.max()) / rms)
+        worst_mean = max(worst_mean, float(err.mean()) / float(np.mean(np.abs(ref))))
+        ids_exact &= bool(np.array_equal(np.asarray(gpu_ids[l]), ids))
+    return {"vs": "oracle (fp64), the layers of the CPU baseline's sample", "layers": len(oracle_layers),
+            "max_err_over_rms": round(worst_max, 6), "mean_rel_err": round(worst_mean, 6),
+            "routing_exact": ids_exact, "bar": {"max_err_over_rms": 2e-2, "mean_rel_err": 5e-3}}
+
+
+def cpu_baseline(wl_name, budget_s=15.0, max_units=None, layers=None, keep=None):
+    """The oracle, as it stands, on the host cores: a bounded sample of the workload.
+    `layers` overrides the workload's layer count; with `keep` (a list) the
+    oracle's output and routing of every whole layer it ran are appended as
+    (layer, out, ids)."""
     import oracle as O
     cfg_name, L = WORKLOADS[wl_name]
+    if layers:
+        L = layers
     cfg = S.CONFIGS[cfg_name]
     t_used = 0.0
     tokens = 0
@@ -396,8 +425,10 @@ def cpu_baseline(wl_name, budget_s=15.0, max_units=None):
             return {k: v[e] for k, v in W.items()}
         if cfg.T <= 64:
             t0 = time.perf_counter()
-            O.layer_forward(x, lg, ge, cfg.E, cfg.d, cfg.f, cfg.k)
+            out, mid = O.layer_forward(x, lg, ge, cfg.E, cfg.d, cfg.f, cfg.k, want_intermediates=True)
             t_used += time.perf_counter() - t0
+            if keep is not None:
+                keep.append((l, out, mid["ids"]))
             tokens += cfg.T
             layers_done += 1
             sample_desc = f"{layers_done} of {L} {cfg.name} layers (T={cfg.T} each), whole layer"
@@ -513,6 +544,10 @@ def main():
     config["l2"] = (f"inputs larger than L2 ({wl.weight_bytes / 1e9:.1f} GB of distinct expert weights "
                     f"across the step; no flush needed)")
     res = measure(M, torch, wl, args.steps, args.warmup, rank, world, peaks, peak_src)
+    want_base = rank == 0 and world == 1 and not args.no_cpu_baseline
+    # the step's outputs and routing, compared with the oracle's below
+    step_out = ([o.cpu() for o in wl.out], [i.cpu().numpy() for i in wl.ids]) if want_base else None
+    n_layers = wl.L
     del wl
     torch.cuda.empty_cache()
 
@@ -529,9 +564,14 @@ def main():
         del wl2
         torch.cuda.empty_cache()
 
-    base = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(args.workload, budget_s=12.0)
+    base = parity = None
+    if want_base:
+        kept = []
+        base = cpu_baseline(args.workload, budget_s=12.0, layers=n_layers, keep=kept)
+        try:
+            parity = parity_vs_oracle(step_out[0], step_out[1], kept) if kept else None
+        except Exception as e:  # the line is still printed
+            parity = {"error": f"{type(e).__name__}: {e}"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(res["value"], 1), "unit": "tokens/s", "n_gpus": world,
@@ -542,6 +582,7 @@ def main():
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
                 "eager_ms_per_step": round(res["eager_ms_per_step"], 4),
                 "stages_us_per_layer": res["stages_us_per_layer"], "uniq_experts_mean": res["uniq_experts_mean"],
+                "parity": parity,
                 "timing": "CUDA graph of the step replayed K times between two events on its stream; "
                           "barrier + synchronize on both sides; max over ranks",
                 "prefill": secondary}

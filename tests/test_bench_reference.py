@@ -63,3 +63,24 @@ def test_reference_arm_under_torchrun_runs_on_rank_0_only():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check_line(lines[0], 2, 1, "decode")
+
+
+def test_bench_parity_fields_on_a_stand_in():
+    """The benchmark's parity entry compares the step's outputs with the
+    oracle's layer by layer: fed the oracle's own outputs rounded to bf16 it
+    reports a rounding-sized error and exact routing, and a changed id is seen."""
+    torch = pytest.importorskip("torch")
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    kept = []
+    base = bench.cpu_baseline("decode", budget_s=2.0, layers=2, keep=kept)
+    assert base["kind"] == "oracle" and len(kept) == 2
+    outs = [torch.from_numpy(o.astype(np.float32)).to(torch.bfloat16) for _, o, _ in kept]
+    ids = [i.copy() for _, _, i in kept]
+    p = bench.parity_vs_oracle(outs, ids, kept)
+    assert p["layers"] == 2 and p["routing_exact"] is True
+    assert 0 < p["max_err_over_rms"] < p["bar"]["max_err_over_rms"]
+    assert 0 < p["mean_rel_err"] < p["bar"]["mean_rel_err"]
+    ids[1][0, 0] ^= 1
+    assert bench.parity_vs_oracle(outs, ids, kept)["routing_exact"] is False
