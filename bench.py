@@ -12,7 +12,11 @@ Metric: MoE-layer tokens/s = tokens routed through the layer per second
 graph of the step on inputs already resident in HBM.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-       [--impl ours|reference] [--no-secondary]
+       [--impl ours|reference] [--layers L] [--no-secondary] [--no-cpu-baseline]
+The JSON line also carries the dominant kernel's roofline, the CPU oracle's
+rate on a bounded sample (cpu_baseline), the parity of the timed step against
+the oracle on that sample, an end-to-end rate with host buffers (e2e), the
+kernel launch count and the SM clocks seen during the timed region.
 Under torchrun (N > 1) every rank runs an independent replica (the layer has
 no cross-GPU exchange); value = all ranks' tokens / max-over-ranks time.
 """
