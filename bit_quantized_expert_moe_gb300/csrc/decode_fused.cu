@@ -2,8 +2,8 @@
 //
 // With T <= 8 tokens the layer is a stream of the routed experts' int4 weights
 // past a handful of activation vectors: "Performance and verification"
-// (bloomery docs/performance.md), section "Why it is fast", reads every routed
-// expert once per batch and takes the dot products on the weights as stored;
+// (bloomery docs/performance.md), section "Why it is fast", fetches each
+// expert's weights once per batch and computes on the packed codes directly;
 // "Measured results" (vllm-omni docs/edge/results.md), section Fidelity, fixes
 // the W4A16 g128 format.  The kernel is built so that the weight stream never
 // waits on anything but routing:

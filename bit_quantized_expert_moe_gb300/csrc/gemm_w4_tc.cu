@@ -1,10 +1,10 @@
 // Stage 3, prefill regime: grouped W4A16 GEMM on the 5th-generation tensor
 // cores (tcgen05, TMEM accumulators, TMA).
 //
-// "Performance and verification", section "Why it is fast": the routed
-// experts of a prompt run as grouped tensor-core GEMMs; "Measured results",
-// section Speed: the prefill path dequantises the 4-bit weights to 16-bit and
-// runs a dense GEMM.  Here the dequantisation happens tile by tile in shared
+// "Performance and verification", section "Why it is fast": a prompt's
+// expert products are batched into grouped tensor-core GEMMs; "Measured
+// results", section Speed: prompts run fastest with the 4-bit weights widened
+// to 16-bit for a dense GEMM.  Here the dequantisation happens tile by tile in shared
 // memory, never in HBM.
 //
 // Shapes (swap-AB: weight rows are the MMA's M, tokens its N):

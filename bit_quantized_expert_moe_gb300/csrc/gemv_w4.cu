@@ -2,8 +2,8 @@
 //
 // With a handful of rows per expert the layer is bound by the bytes of the
 // experts' weights, which are read exactly once ("Performance and
-// verification", section "Why it is fast": each routed expert of a batch is
-// read once; dot products on the quantized weights as stored).
+// verification", section "Why it is fast": one fetch of an expert per batch;
+// the packed 4-bit codes enter the arithmetic without being expanded first).
 //
 // Layout of the work:
 //   * a thread owns one 32-element chunk c of the reduction axis (16 bytes of

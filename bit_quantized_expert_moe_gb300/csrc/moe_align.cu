@@ -1,7 +1,7 @@
 // Stage 2: token -> expert permutation (stable counting sort) and gather.
 //
-// The assignments a = t*k + j are grouped by expert so that each expert's
-// weights are read once for the whole batch ("Performance and verification",
+// The assignments a = t*k + j are grouped by expert so that the weights of an
+// expert are fetched a single time per batch ("Performance and verification",
 // section "Why it is fast").  Inside an expert's segment the assignments keep
 // ascending a (a stable sort), so the permutation is unique and is compared
 // bit-exactly.

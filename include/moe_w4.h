@@ -94,7 +94,8 @@ typedef struct {
 
 /*
  * Stage 1 -- top-k routing.  "Performance and verification", section
- * "How it is verified": router ids are integer outputs compared exactly.
+ * "How it is verified": the chosen expert ids are integers, checked for
+ * exact equality.
  *
  * For each token t: the k experts with the largest logits, slot 0 the largest,
  * equal logits ordered by ascending expert id; the comparison is exact on the
@@ -110,8 +111,8 @@ moe_status_t moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k
 
 /*
  * Stage 2 -- token -> expert permutation.  "Performance and verification",
- * section "Why it is fast": each routed expert a batch calls is read once for
- * the whole batch, so assignments are grouped by expert first.
+ * section "Why it is fast": an expert's weights are fetched a single time per
+ * batch, so assignments are grouped by expert first.
  *
  * Assignment a = t*k + j goes to expert topk_ids[a].  Outputs:
  *   counts  [E]    assignments per expert
@@ -166,7 +167,7 @@ moe_status_t moe_permute_noalloc(const int32_t* topk_ids, int32_t T, int32_t k, 
 /*
  * Stage 3 -- grouped expert FFN on the permuted rows.  "Performance and
  * verification", section "Why it is fast" (grouped tensor-core GEMMs for the
- * routed experts of a prompt; dot products on the weights as stored) and
+ * routed experts of a prompt; arithmetic directly on the packed codes) and
  * "Measured results", section Speed (W4A16 g128; prefill dequantises to
  * 16-bit for a dense GEMM).
  *

@@ -17,9 +17,10 @@ layer; they fix the weight format and the shape of the computation:
     per group of 128), 4-bit codes stored packed eight to a 32-bit word
     (`unpack_nibbles` expands them 8x into int32).
   * "Performance and verification" (bloomery docs/performance.md), section
-    "Why it is fast": every routed expert a batch calls is read once for the
-    whole batch; routed experts run as grouped GEMMs; section "How it is
-    verified": router ids must match exactly outside tie bands.
+    "Why it is fast": the tokens of a batch are grouped by expert so that an
+    expert's weights are fetched a single time per batch, and the experts'
+    matrix products are grouped; section "How it is verified": the router's
+    expert ids are integers and are held to exact equality (ties aside).
 The remaining definitions are the plainest reading of the problem statement:
 top-k by descending logit with ties to the lower expert id, combine weights =
 softmax over the k selected logits, SiLU(gate) * up, a stable counting-sort
