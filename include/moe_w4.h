@@ -11,10 +11,11 @@
  *
  * Sources for what each call computes:
  *   - "Performance and verification" (bloomery docs/performance.md), section
- *     "Why it is fast": a batch reads every routed expert it calls once for
- *     the whole batch; routed experts of a prompt run as grouped tensor-core
- *     GEMMs; CPU experts take their dot products on the quantized weights as
- *     stored.  Section "How it is verified": router ids match exactly.
+ *     "Why it is fast": grouping a batch by expert means one fetch of each
+ *     expert's weights per batch; a prompt's expert products are batched into
+ *     grouped tensor-core GEMMs; the host computes on the packed 4-bit codes
+ *     without expanding them.  Section "How it is verified": expert ids are
+ *     integers held to exact equality.
  *   - "Measured results" (vllm-omni docs/edge/results.md), sections Speed and
  *     Fidelity: W4A16 with groups of 128, 4.25 bits per weight; the prefill
  *     path dequantises to 16-bit and runs a dense GEMM.
