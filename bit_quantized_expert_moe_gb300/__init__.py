@@ -27,7 +27,7 @@ MOE_OK = 0
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_MISALIGNED", 3: "MOE_ERR_UNSUPPORTED",
     4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_RANGE", 7: "MOE_ERR_TIMEOUT",
-    8: "MOE_ERR_F16_RANGE", 9: "MOE_ERR_SCRATCH_LIMIT",
+    8: "MOE_ERR_F16_RANGE", 9: "MOE_ERR_SCRATCH_LIMIT", 10: "MOE_ERR_CAPTURE",
 }
 
 

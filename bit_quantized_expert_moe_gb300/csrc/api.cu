@@ -222,6 +222,7 @@ const char* moe_status_str(moe_status_t s) {
         case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
         case MOE_ERR_F16_RANGE: return "MOE_ERR_F16_RANGE";
         case MOE_ERR_SCRATCH_LIMIT: return "MOE_ERR_SCRATCH_LIMIT";
+        case MOE_ERR_CAPTURE: return "MOE_ERR_CAPTURE";
     }
     return "MOE_ERR_UNKNOWN";
 }

@@ -662,8 +662,13 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
                 ++round;
             }
         };
+        // A consumer that gave up releases its slot without the chunk having
+        // landed, and only once the abort flag is raised; so a slot wait that
+        // completes with the flag raised issues nothing more, and the drain of
+        // each slot's last use below then covers every copy still in flight.
         auto slot_free = [&](uint32_t slot) -> int {
-            return round == 0 || tc::mbar_wait(empty0 + 8u * slot, (round - 1) & 1u, abort_flag, p.err);
+            if (round != 0 && !tc::mbar_wait(empty0 + 8u * slot, (round - 1) & 1u, abort_flag, p.err)) return 0;
+            return *abort_flag ? 0 : 1;
         };
         // A pair's position in its chunk range: chunk c of tile (p0, p1) =
         // (touched-expert index, feature block) in phase 1, (unit, slot j) in
@@ -1136,8 +1141,8 @@ bool plan_layout(int T, int k, int E, int d, int f, int G, int nq, Layout* L) {
 }  // namespace
 
 // Pipelines for a layer: 3 while the routed weights per CTA are small (at most
-// T k experts touched), else 4 (both measured on the BASELINE-shaped layers:
-// 12 consumer warps win at d_model 2048, 16 at d_model 7168).
+// T k experts touched), else 4 (both measured on the benchmark workloads'
+// shapes: 12 consumer warps win at d_model 2048, 16 at d_model 7168).
 int pick_nq(int T, int k, int E, int d, int f, int G) {
     const double bytes = (double)std::min(T * k, E) * 3.0 * d * f * 0.53125 / G;
     return bytes <= 1.0e6 ? 3 : 4;

@@ -20,7 +20,8 @@
 // The array's name is only a host-side stand-in for the device copy, so the
 // device address is looked up once per device with cudaGetSymbolAddress (on
 // the first call made with that device current) and cached.  Make that first
-// call before any stream capture.
+// call before any stream capture: a first call on a capturing stream returns
+// MOE_ERR_CAPTURE and does nothing.
 #include <mutex>
 
 #include "internal.h"
@@ -37,11 +38,18 @@ std::mutex g_scratch_mu;
 void* g_scratch_dev[NOALLOC_MAX_DEVICES] = {};
 
 // Device address of the scratch array on the current device (looked up once).
-moe_status_t scratch_address(unsigned char** out) {
+// The lookup may load the library's device code, which a stream capture in
+// progress would not allow (it could invalidate the caller's capture), so a
+// first call made on a capturing stream is refused with MOE_ERR_CAPTURE before
+// any CUDA call other than the capture query.
+moe_status_t scratch_address(cudaStream_t stream, unsigned char** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_dev[dev]) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return MOE_ERR_CAPTURE;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
         g_scratch_dev[dev] = p;
@@ -93,7 +101,7 @@ extern "C" moe_status_t moe_permute_noalloc(const int32_t* topk_ids, int32_t T, 
     const NoallocLayout l = layout(R, E);
     if (l.end > sizeof(g_permute_scratch)) return MOE_ERR_SCRATCH_LIMIT;
     unsigned char* base = nullptr;
-    moe_status_t st = scratch_address(&base);
+    moe_status_t st = scratch_address(stream, &base);
     if (st != MOE_OK) return st;
     AlignOut o{counts,
                offsets,

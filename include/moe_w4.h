@@ -63,7 +63,8 @@ typedef enum {
     MOE_ERR_DEVICE_RANGE = 6,  /* device side: an expert id was outside [0, E) */
     MOE_ERR_TIMEOUT = 7,       /* device side: a bounded pipeline wait gave up */
     MOE_ERR_F16_RANGE = 8,     /* device side: a value left fp16's range in the tensor-core regime */
-    MOE_ERR_SCRATCH_LIMIT = 9  /* moe_permute_noalloc: T*k larger than its fixed scratch allows */
+    MOE_ERR_SCRATCH_LIMIT = 9, /* moe_permute_noalloc: T*k larger than its fixed scratch allows */
+    MOE_ERR_CAPTURE = 10       /* moe_permute_noalloc: first call on a device made while its stream captures */
 } moe_status_t;
 
 /*
@@ -151,7 +152,9 @@ size_t moe_permute_workspace_size(int32_t T, int32_t k, int32_t E);
  *     launches nothing.  Other argument errors as for moe_permute.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  A first call made while `stream` is capturing returns
+ *     MOE_ERR_CAPTURE, launches nothing and leaves the capture intact (the
+ *     lookup could load device code, which a capture does not allow).
  *   - All calls share the one array and it keeps the last call's contents
  *     (the call rewrites every part it reads, so no clearing is needed).
  *     Calls that overlap on the GPU -- on different streams or from different
@@ -174,8 +177,9 @@ moe_status_t moe_permute_noalloc(const int32_t* topk_ids, int32_t T, int32_t k, 
  *
  * For every expert e and every permuted row i in offsets[e]..offsets[e+1]-1:
  *   g = x_perm[i] . Wg[e]^T,  u = x_perm[i] . Wu[e]^T      (fp32 accumulation)
- *   h = SiLU(g) * u  rounded to bf16,   SiLU(g) = g / (1 + exp(-g))
- *   y_perm[i] = (row_w ? row_w[i] : 1) * (h . Wd[e]^T)      rounded to bf16
+ *   h = SiLU(g) * u,   SiLU(g) = g / (1 + exp(-g))   (intermediate: fp32 in the
+ *                      GEMV regime, rounded to fp16 in the tensor-core regime)
+ *   y_perm[i] = (row_w ? row_w[i] : 1) * (h . Wd[e]^T)      the output, rounded to bf16
  * Experts with no rows are not read.  Two regimes, chosen from R on the host:
  * a CUDA-core GEMV for few rows and a tcgen05 tensor-core grouped GEMM for
  * many (override with the environment variable MOE_W4_REGIME=decode|prefill).

@@ -211,25 +211,16 @@ def _run_layer(M, cfg, layer_idx=0):
     return W, x, lg, ids.cpu().numpy(), bf16_to_f64(out)
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large_decode"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skew", "large_decode", "large_prefill"])
 def test_layer_forward_full(M, name):
+    """Every output element of the whole layer at each workload's full size
+    (the oracle's cost is dominated by dequantising the touched experts, so the
+    4096-token skewed layer and the 512-token large layer are affordable)."""
     cfg = S.CONFIGS[name]
     W, x, lg, ids, out = _run_layer(M, cfg)
     ref, inter = OM.layer_forward(x, lg, _getter(W), cfg.E, cfg.d, cfg.f, cfg.k, want_intermediates=True)
     assert np.array_equal(ids, inter["ids"])
-    assert_close(out, ref, name)
-
-
-@pytest.mark.parametrize("name,ntok", [("skew", 48), ("large_prefill", 6)])
-def test_layer_forward_sampled(M, name, ntok):
-    cfg = S.CONFIGS[name]
-    W, x, lg, ids, out = _run_layer(M, cfg)
-    ids_ref, _ = OM.route_topk(lg, cfg.k)
-    assert np.array_equal(ids, ids_ref)
-    rng = np.random.default_rng(11)
-    toks = np.sort(rng.choice(cfg.T, size=ntok, replace=False))
-    ref = OM.layer_forward_tokens(x, lg, _getter(W), cfg.E, cfg.d, cfg.f, cfg.k, toks)
-    assert_close(out[toks], ref, name)
+    assert_close(out, ref, f"layer {name}")
 
 
 def test_decode_layers_of_the_stack(M):
@@ -398,6 +389,11 @@ def test_fused_decode_back_to_back_calls_on_one_workspace(M, name):
         calls[l](xs[l], lgs[l], o)
         torch.cuda.synchronize()
         ref.append(o)
+        # the single calls are themselves held to the oracle
+        W = _layer(cfg, l)
+        ora = OM.layer_forward(S.activations(cfg, l), S.router_logits(cfg, l), _getter(W), cfg.E, cfg.d, cfg.f,
+                               cfg.k)
+        assert_close(bf16_to_f64(o), ora, f"{name} layer {l}, single call")
     seq = [i % nl for i in range(24)]
     outs = [torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda") for _ in seq]
     for o, l in zip(outs, seq):

@@ -1,9 +1,14 @@
-"""Helpers shared by the tests: device upload and the parity tolerance."""
+"""Helpers shared by the tests: device upload, the parity tolerance and a log
+of the measured errors (printed at the end of the run by conftest.py)."""
 import numpy as np
 
 # Parity bar for bf16 outputs against the fp64 oracle.
 MAX_ERR_OVER_RMS = 2e-2
 MEAN_REL_ERR = 5e-3
+
+# (label, max|err|/rms(ref), mean|err|/mean|ref|, worst err/bar) of every
+# assert_close call of this process, in call order.
+PARITY_LOG = []
 
 
 def build_lib():
@@ -34,8 +39,8 @@ def bf16_to_f64(t):
 
 
 def bf16_half_ulp(ref):
-    """Half the spacing of bf16 numbers at |ref| (the rounding error bound of a
-    correctly rounded bf16 value)."""
+    """Half the spacing of bf16 numbers at |ref|: the largest error of the
+    correctly rounded bf16 value of ref."""
     a = np.abs(np.asarray(ref, np.float64))
     e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
     return np.where(a > 0, 2.0 ** (e - 8), 0.0)
@@ -46,9 +51,12 @@ def err_stats(got, ref):
     ref = np.asarray(ref, np.float64)
     err = np.abs(got - ref)
     rms = float(np.sqrt(np.mean(ref ** 2)))
-    # Per-element bar: 2e-2 rms(ref), except that no element is held below its
-    # own bf16 rounding step (half an ulp at |ref|, plus 1e-3 |ref| of slack).
-    bar = np.maximum(MAX_ERR_OVER_RMS * rms, bf16_half_ulp(ref) + 1e-3 * np.abs(ref))
+    # Per-element bar: 2e-2 rms(ref), raised to half a bf16 ulp of ref where
+    # that is larger.  A bf16 output cannot do better than its own rounding
+    # step: on the 512-token prefill layer the fp64 oracle rounded to bf16 and
+    # nothing else is already 0.02057 rms(ref) off at its largest outputs
+    # (6.65 rms), so the literal bar alone would reject the exact answer.
+    bar = np.maximum(MAX_ERR_OVER_RMS * rms, bf16_half_ulp(ref))
     return {
         "max_err_over_rms": float(err.max() / rms) if rms > 0 else float(err.max()),
         "mean_rel_err": float(err.mean() / np.abs(ref).mean()) if np.abs(ref).mean() > 0 else float(err.mean()),
@@ -59,7 +67,9 @@ def err_stats(got, ref):
 
 def assert_close(got, ref, what=""):
     """The parity bar for bf16 outputs: every element within its bar (see
-    err_stats) and mean|err| / mean|ref| <= 5e-3."""
+    err_stats) and mean|err| / mean|ref| <= 5e-3.  The literal max|err|/rms is
+    logged for the end-of-run report."""
     s = err_stats(got, ref)
+    PARITY_LOG.append((what, s["max_err_over_rms"], s["mean_rel_err"], s["worst_err_over_bar"]))
     assert s["worst_err_over_bar"] <= 1.0 and s["mean_rel_err"] <= MEAN_REL_ERR, (what, s)
     return s
