@@ -51,25 +51,34 @@ def err_stats(got, ref):
     ref = np.asarray(ref, np.float64)
     err = np.abs(got - ref)
     rms = float(np.sqrt(np.mean(ref ** 2)))
-    # Per-element bar: 2e-2 rms(ref), raised to half a bf16 ulp of ref where
-    # that is larger.  A bf16 output cannot do better than its own rounding
-    # step: on the 512-token prefill layer the fp64 oracle rounded to bf16 and
-    # nothing else is already 0.02057 rms(ref) off at its largest outputs
-    # (6.65 rms), so the literal bar alone would reject the exact answer.
-    bar = np.maximum(MAX_ERR_OVER_RMS * rms, bf16_half_ulp(ref))
+    # Per-element bar: the literal 2e-2 rms(ref) wherever a bf16 value can meet
+    # it, i.e. wherever half a bf16 ulp of ref is at most 2e-2 rms(ref).  At the
+    # few elements where it is not (on the 512-token prefill layer the fp64
+    # oracle rounded to bf16 and nothing else is already 0.02057 rms(ref) off
+    # at its largest outputs), the output must be faithfully rounded: one of
+    # the two bf16 values that bracket ref, |err| < one ulp.  Correct rounding
+    # cannot be asked there: the closest of those elements lies 0.0009 rms(ref)
+    # from a rounding midpoint, below the rounding error of any 16-bit
+    # intermediate.
+    hu = bf16_half_ulp(ref)
+    lit = MAX_ERR_OVER_RMS * rms
+    bar = np.where(hu > lit, 2.0 * hu, lit)
     return {
         "max_err_over_rms": float(err.max() / rms) if rms > 0 else float(err.max()),
         "mean_rel_err": float(err.mean() / np.abs(ref).mean()) if np.abs(ref).mean() > 0 else float(err.mean()),
         "worst_err_over_bar": float((err / bar).max()) if rms > 0 else 0.0,
+        "n_over_literal": int((err > lit).sum()),
         "rms_ref": rms,
     }
 
 
 def assert_close(got, ref, what=""):
     """The parity bar for bf16 outputs: every element within its bar (see
-    err_stats) and mean|err| / mean|ref| <= 5e-3.  The literal max|err|/rms is
+    err_stats; strictly below one ulp where the literal bar is out of bf16's
+    reach) and mean|err| / mean|ref| <= 5e-3.  The literal max|err|/rms is
     logged for the end-of-run report."""
     s = err_stats(got, ref)
-    PARITY_LOG.append((what, s["max_err_over_rms"], s["mean_rel_err"], s["worst_err_over_bar"]))
-    assert s["worst_err_over_bar"] <= 1.0 and s["mean_rel_err"] <= MEAN_REL_ERR, (what, s)
+    PARITY_LOG.append((what, s["max_err_over_rms"], s["mean_rel_err"], s["worst_err_over_bar"],
+                       s["n_over_literal"]))
+    assert s["worst_err_over_bar"] < 1.0 and s["mean_rel_err"] <= MEAN_REL_ERR, (what, s)
     return s
