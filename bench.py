@@ -189,6 +189,12 @@ class Workload:
         return self.cfg.T * self.L
 
 
+def decode_kernel_name():
+    """The one-kernel decode layer the library runs (MOE_W4_DECODE_KERNEL=flow
+    picks the dataflow kernel instead of the default grid-barrier kernel)."""
+    return "decode_flow_kernel" if os.environ.get("MOE_W4_DECODE_KERNEL") == "flow" else "decode_fused_kernel"
+
+
 def expert_bytes(cfg, which):
     """Algorithmic bytes of one expert's gate_up or down matrix (codes + fp16 scale + zero)."""
     n = (2 * cfg.f * cfg.d) if which == "gate_up" else (cfg.d * cfg.f)
@@ -287,8 +293,8 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
         t_lay = np.full(wl.L, ms / wl.L / 1e3)
         achieved = float(lay_bytes.sum() / t_lay.sum() / 1e9)
         peak = float(peaks["hbm_gbs"])
-        tr = traffic_for("decode_fused_" + wl.name)
-        roofline = {"bound": "hbm", "kernel": "decode_fused_kernel", "achieved": round(achieved, 1),
+        tr = traffic_for(decode_kernel_name().replace("_kernel", "") + "_" + wl.name)
+        roofline = {"bound": "hbm", "kernel": decode_kernel_name(), "achieved": round(achieved, 1),
                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                     "traffic": (round(tr["dram_bytes_per_launch"]) if tr else None),
                     "algorithmic_bytes_per_launch": round(float(lay_bytes.mean())),
@@ -334,7 +340,7 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
         # one launch holds every stage: only the bracket around it means
         # anything (its event-record nodes also stop consecutive launches from
         # overlapping, so it reads above the timed region's per-layer time)
-        stages = {"decode_fused_kernel (routing .. combine, event-bracketed)":
+        stages = {f"{decode_kernel_name()} (routing .. combine, event-bracketed)":
                   round(float(stage_sum[0]) * 1e3 / wl.L, 2)}
     else:
         stages = {k: round(float(v) * 1e3 / wl.L, 2) for k, v in
@@ -403,6 +409,27 @@ def parity_vs_oracle(gpu_out, gpu_ids, oracle_layers):
     return {"vs": "oracle (fp64), the layers of the CPU baseline's sample", "layers": len(oracle_layers),
             "max_err_over_rms": round(worst_max, 6), "mean_rel_err": round(worst_mean, 6),
             "routing_exact": ids_exact, "bar": {"max_err_over_rms": 2e-2, "mean_rel_err": 5e-3}}
+
+
+def sampled_parity(wl, ntok):
+    """The measured step's outputs of the workload's first layer against the
+    oracle: routing ids of every token exactly, outputs of `ntok` sampled
+    tokens within the bar (max|err|/rms of the sample, mean relative error)."""
+    import oracle as O
+    cfg = wl.cfg
+    x, lg, W = wl.host_x[0], wl.host_lg[0], wl.host_w[0]
+    ids_ref, _ = O.route_topk(lg, cfg.k)
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(cfg.T, size=min(ntok, cfg.T), replace=False))
+    ref = O.layer_forward_tokens(x, lg, lambda e: {k: v[e] for k, v in W.items()}, cfg.E, cfg.d, cfg.f, cfg.k, toks)
+    got = bf16_host_to_f64(wl.out[0].cpu())[toks]
+    err = np.abs(got - ref)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return {"vs": "oracle (fp64)", "tokens": int(len(toks)), "of": int(cfg.T),
+            "max_err_over_rms": round(float(err.max()) / rms, 6),
+            "mean_rel_err": round(float(err.mean()) / float(np.mean(np.abs(ref))), 6),
+            "routing_exact": bool(np.array_equal(wl.ids[0].cpu().numpy(), ids_ref)),
+            "bar": {"max_err_over_rms": 2e-2, "mean_rel_err": 5e-3}}
 
 
 def cpu_baseline(wl_name, budget_s=15.0, max_units=None, layers=None, keep=None):
@@ -555,18 +582,34 @@ def main():
     del wl
     torch.cuda.empty_cache()
 
-    secondary = None
+    # Every other workload of the suite, each with its own roofline, end-to-end
+    # rate, clocks and a sampled parity check against the oracle.  "prefill"
+    # keeps the skewed P=4096 layer (the prefill headline); "workloads" holds
+    # the 512-token prefill layer and the large decode and prefill layers.
+    secondary, others = None, {}
     if not args.no_secondary and args.workload == "decode":
-        wl2 = Workload(M, torch, "skew", dev)
-        steps2 = max(5, args.steps)
-        r2 = measure(M, torch, wl2, steps2, args.warmup, rank, world, peaks, peak_src, want_e2e=True)
-        secondary = {"workload": "skew: one prefill layer, P=4096, Zipf(1.1) load, d_model=2048, d_ff=768, E=128, top-8",
+        for name, nl, ntok in (("skew", None, 16), ("prefill", None, 16), ("large_decode", 4, 2),
+                               ("large_prefill", None, 4)):
+            wl2 = Workload(M, torch, name, dev, layers=nl)
+            steps2 = max(5, args.steps)
+            r2 = measure(M, torch, wl2, steps2, args.warmup, rank, world, peaks, peak_src, want_e2e=True)
+            entry = {"workload": f"{name}: {wl2.cfg.name} layer x{wl2.L}, T={wl2.cfg.T}, d_model={wl2.cfg.d}, "
+                                 f"d_ff={wl2.cfg.f}, E={wl2.cfg.E}, top-{wl2.cfg.k}",
                      "value": round(r2["value"], 1), "unit": "tokens/s", "ms_per_step": round(r2["ms_per_step"], 4),
                      "eager_ms_per_step": round(r2["eager_ms_per_step"], 4), "roofline": r2["roofline"],
                      "stages_us_per_layer": r2["stages_us_per_layer"], "gpu_launches": r2["gpu_launches"],
-                     "clocks": r2["clocks"], "e2e": r2["e2e"]}
-        del wl2
-        torch.cuda.empty_cache()
+                     "clocks": r2["clocks"], "e2e": r2["e2e"], "uniq_experts_mean": r2["uniq_experts_mean"]}
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                try:
+                    entry["parity"] = sampled_parity(wl2, ntok)
+                except Exception as e:  # the line is still printed
+                    entry["parity"] = {"error": f"{type(e).__name__}: {e}"}
+            if name == "skew":
+                secondary = entry
+            else:
+                others[name] = entry
+            del wl2
+            torch.cuda.empty_cache()
 
     base = parity = None
     if want_base:
@@ -589,7 +632,7 @@ def main():
                 "parity": parity,
                 "timing": "CUDA graph of the step replayed K times between two events on its stream; "
                           "barrier + synchronize on both sides; max over ranks",
-                "prefill": secondary}
+                "prefill": secondary, "workloads": others or None}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()

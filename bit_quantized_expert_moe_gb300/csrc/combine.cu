@@ -24,25 +24,37 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int pos = inv[(size_t)t * k + j];
-            if ((unsigned)pos >= (unsigned)(T * k)) continue;  // not a permutation entry
-            const float wj = w[(size_t)t * k + j];
-            const uint4 v = *reinterpret_cast<const uint4*>(y_perm + (size_t)pos * d + c * 8);
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        // slots in batches of 8: every row load of a batch is in flight
+        // before the first is used; the sum still runs in slot order
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            uint4 v[8];
+            float wj[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float lo, hi;
-                if (Y_F16) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
-                    lo = f.x;
-                    hi = f.y;
-                } else {
-                    lo = __uint_as_float(u[i] << 16);
-                    hi = __uint_as_float(u[i] & 0xFFFF0000u);
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = j0 + jj;
+                const int pos = j < k ? inv[(size_t)t * k + j] : -1;
+                const bool ok = (unsigned)pos < (unsigned)(T * k);  // else not a permutation entry
+                wj[jj] = ok ? w[(size_t)t * k + j] : 0.f;
+                v[jj] = ok ? *reinterpret_cast<const uint4*>(y_perm + (size_t)pos * d + c * 8) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                if (j0 + jj >= k) break;
+                const uint32_t u[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float lo, hi;
+                    if (Y_F16) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+                        lo = f.x;
+                        hi = f.y;
+                    } else {
+                        lo = __uint_as_float(u[i] << 16);
+                        hi = __uint_as_float(u[i] & 0xFFFF0000u);
+                    }
+                    acc[2 * i] = fmaf(wj[jj], lo, acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(wj[jj], hi, acc[2 * i + 1]);
                 }
-                acc[2 * i] = fmaf(wj, lo, acc[2 * i]);
-                acc[2 * i + 1] = fmaf(wj, hi, acc[2 * i + 1]);
             }
         }
         uint4 o;

@@ -10,7 +10,8 @@
 //
 //   phase 0  every CTA routes all T tokens itself (top-k of the logits held
 //            in shared memory, softmax over the selection) and sorts the T*k
-//            assignments by expert, so no CTA waits for another to learn which
+//            assignments by expert (a rank per assignment from comparisons
+//            with all the others), so no CTA waits for another to learn which
 //            experts are needed.  CTA 0 writes the routing to topk_ids_out.
 //   phase 1  gate_up: the CTA takes a contiguous share of the tiles
 //            (touched expert u, 8 features) and computes, for each token routed
@@ -54,13 +55,13 @@
 #include <cfloat>
 #include <climits>
 
+#include "decode_ops.cuh"
 #include "fastdiv.h"
-#include "internal.h"
-#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
 
+using namespace dec;
 using tc::WAIT_LIMIT_NS;
 
 // Warp layout of one instantiation: NQ producer pipelines (producer warp
@@ -78,12 +79,6 @@ struct Shape {
     static constexpr int NTHREADS = 32 * (CW + NQ_);
     static constexpr int CONSUMER_THREADS = 32 * CW;
 };
-constexpr int LINES = 4;                        // 128-byte lines (2 groups each) per chunk row
-constexpr int CHUNK_GROUPS = 2 * LINES;         // groups of 128 codes per chunk
-constexpr int BOX_BYTES = 8 * LINES * 128;      // 8 rows x 4 lines (rows g; rows g + 8 follow)
-constexpr int SLOT_CODE = 2 * BOX_BYTES;        // one TMA box: 16 rows of codes (a multiple of the 1024-byte swizzle atom)
-constexpr int SZ_ARRAY = 16 * CHUNK_GROUPS * 2; // fp16 [16 rows][8 groups]
-constexpr int SLOT_SZ = 2 * SZ_ARRAY;           // scales, then zeros
 constexpr uint32_t FULL_ARRIVALS = 1;          // lane 0's expect_tx arrival (cp.async arrivals are counted)
 // Each pipeline numbers its chunks in issue order and indexes its "full"
 // barriers by chunk number modulo NFQ (not by ring slot: the pipeline's two
@@ -96,10 +91,6 @@ constexpr uint32_t FULL_ARRIVALS = 1;          // lane 0's expect_tx arrival (cp
 // and the barrier's parity names q's phase unambiguously.
 constexpr int NFQ = 64;
 static_assert((NFQ & (NFQ - 1)) == 0, "NFQ must be a power of two");
-constexpr int MAX_T = 8;
-constexpr int MAX_R = 64;
-constexpr int ROW_PAD = 64;                     // bytes after each staged activation row
-constexpr size_t SMEM_LIMIT = 232448;
 constexpr int MAX_SLOTS = 32;
 
 struct Tab {
@@ -110,6 +101,7 @@ struct Tab {
     int32_t uexp[MAX_R];   // touched experts, ascending
     int32_t uoff[MAX_R];
     int32_t ucnt[MAX_R];
+    int32_t first[MAX_R];  // sort scratch: 1 if assignment a is its expert's first
     int32_t n_uniq;
     int32_t abort;
     int32_t pad[30];
@@ -127,7 +119,6 @@ struct Params {
     int T, k, E, d, f;
     int nslot;                 // a multiple of the pipeline count NQ: pipeline i owns slots [i, i + 1) * nslot / NQ
     uint32_t off_sz, off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab;
-    uint32_t off_cnt;          // phase-0 counters inside the ring, after the logits
     int xb_stride, hs_stride;  // bytes per staged row
     // how the scales and zeros of gate_up / down reach a slot (SZ_*) and their
     // row stride there in bytes
@@ -138,231 +129,6 @@ struct Params {
     FastDiv fd_G, fd_T, fd_nct0, fd_nct1, fd_nch1, fd_nch2, fd_nfb1, fd_k, fd_ns4;
     FastDiv fd_xw, fd_hw;  // 16-byte words per activation row (d / 8) and per h row (f / 8)
 };
-
-// Scales and zeros of a chunk: by TMA boxes where a row of groups is a
-// multiple of 16 bytes (groups % 8 == 0; [16 rows][8 groups] in the slot), by
-// plain bulk copies where a whole row fits one chunk (the chunk's rows are
-// then contiguous: [16 rows][groups] in the slot), else by 4-byte cp.async.
-enum { SZ_CPASYNC = 0, SZ_TMA = 1, SZ_BULK = 2 };
-
-// ------------------------------------------------------------ small helpers
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ float2 lds_f2(uint32_t a) {
-    float2 v;
-    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
-    uint16_t h;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
-    return h;
-}
-// 16-byte shared load done only by lanes with `active` set (others get zeros):
-// lanes that skip it issue no shared-memory wavefronts.
-__device__ __forceinline__ uint4 lds128_if(uint32_t a, uint32_t active) {
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %5, 0;\n\t"
-        "@p ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
-        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w) : "r"(a), "r"(active));
-    return v;
-}
-__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" :: "r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
-}
-__device__ __forceinline__ uint4 ldg_cg16(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
-__device__ __forceinline__ uint64_t ld_acquire_gpu64(const unsigned long long* p) {
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint64_t atom_add_release_gpu(unsigned long long* p, uint64_t v) {
-    uint64_t old;
-    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-    return old;
-}
-__device__ __forceinline__ void bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
-}
-
-// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulation.
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// ------------------------------------------------------------------ routing
-// Order-preserving map of a finite fp32 value to uint32 (larger value, larger
-// key; -0 is folded onto +0 so that equal values give equal keys).  Every
-// finite value maps above 0x007FFFFF, so 0 can stand for "no candidate".
-__device__ __forceinline__ uint32_t route_key(float v) {
-    if (v == 0.0f) v = 0.0f;
-    const uint32_t b = __float_as_uint(v);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// Top-k of one token by one warp, logits read once from shared memory (`row`)
-// into registers (VPL per lane: experts lane, lane+32, ...): k rounds of
-// (warp maximum of the keys, then the lowest expert id among the lanes
-// holding it), i.e. a sort by (-logit, id) on the exact fp32 values (router
-// ids must match exactly: "Performance and verification", section "How it is
-// verified").  Lane j (and j+32) keeps slot j; the weights are the softmax of
-// the k <= 64 selected logits, in fp32.  No shared-memory traffic and no
-// data-dependent branch inside the rounds.
-template <int VPL>
-__device__ __forceinline__ void route_token_regs(const float* row, int E, int k, int32_t* out_ids, float* out_w) {
-    const int lane = threadIdx.x & 31;
-    uint32_t key[VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        key[i] = e < E ? route_key(row[e]) : 0u;
-    }
-    float vmax = 0.f, v0 = 0.f, v1 = 0.f;
-    int id0 = 0, id1 = 0;
-    for (int j = 0; j < k; ++j) {
-        uint32_t bk = key[0];
-        int bi = 0;
-#pragma unroll
-        for (int i = 1; i < VPL; ++i) {
-            const bool better = key[i] > bk;  // ascending e within the lane: ties keep the lower id
-            bk = better ? key[i] : bk;
-            bi = better ? i : bi;
-        }
-        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
-        const int win = __reduce_min_sync(0xffffffffu, (bk == kmax && bk != 0u) ? lane + 32 * bi : INT_MAX);
-        const bool mine = (win & 31) == lane;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) key[i] = (mine && i == (win >> 5)) ? 0u : key[i];
-        // the winning key back to its value (route_key is invertible on finite values)
-        const float v = __uint_as_float((kmax & 0x80000000u) ? (kmax & 0x7FFFFFFFu) : ~kmax);
-        vmax = (j == 0) ? v : vmax;
-        if (lane == j) { id0 = win; v0 = v; }
-        if (lane + 32 == j) { id1 = win; v1 = v; }
-    }
-    const float ex0 = lane < k ? expf(v0 - vmax) : 0.f;
-    const float ex1 = lane + 32 < k ? expf(v1 - vmax) : 0.f;
-    float sum = ex0;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (k > 32) {
-        float s1 = ex1;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, off);
-        sum += s1;
-    }
-    const float inv_sum = 1.0f / sum;
-    if (lane < k) {
-        out_ids[lane] = id0;
-        out_w[lane] = ex0 * inv_sum;
-    }
-    if (lane + 32 < k) {
-        out_ids[lane + 32] = id1;
-        out_w[lane + 32] = ex1 * inv_sum;
-    }
-    __syncwarp();
-}
-
-__device__ __forceinline__ void route_token(const float* row, int E, int k, int32_t* out_ids, float* out_w) {
-    const int nv = (E + 31) >> 5;
-    if (nv <= 1) route_token_regs<1>(row, E, k, out_ids, out_w);
-    else if (nv <= 2) route_token_regs<2>(row, E, k, out_ids, out_w);
-    else if (nv <= 4) route_token_regs<4>(row, E, k, out_ids, out_w);
-    else if (nv <= 8) route_token_regs<8>(row, E, k, out_ids, out_w);
-    else if (nv <= 16) route_token_regs<16>(row, E, k, out_ids, out_w);
-    else route_token_regs<32>(row, E, k, out_ids, out_w);
-}
-
-// -------------------------------------------------------- staged activations
-// Position of word w (0..15) of a group inside a staged activation row: the
-// four words a thread reads in turn land in four different bank quads.
-__device__ __forceinline__ int stage_word(int w) { return (w & 12) | ((w ^ (w >> 2)) & 3); }
-
-// Byte offset of feature (or input column) c inside a staged row: group c/128
-// (256 bytes), word (c/8)%16 at stage_word, then the eight values of the word
-// in the order 0,4,1,5,2,6,3,7 (the k-pairs of the MMA's B fragment).
-__device__ __forceinline__ uint32_t staged_offset(int c) {
-    return (uint32_t)((c >> 7) * 256 + stage_word((c >> 3) & 15) * 16 + k8_pos(c & 7) * 2);
-}
-
-// A staged word's contributions to (C1, C2).
-__device__ __forceinline__ float2 word_c1c2(uint4 o) {
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&o.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&o.y));
-    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&o.z));
-    const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&o.w));
-    const float even = (a.x + a.y) + (c.x + c.y);  // k = 0, 4, 2, 6
-    const float odd = (b.x + b.y) + (e.x + e.y);   // k = 1, 5, 3, 7
-    return make_float2(1024.0f * even + 64.0f * odd, even + odd);
-}
-// Sum over the 16 lanes of a half-warp (one group of 16 words).
-__device__ __forceinline__ float2 halfwarp_sum(float2 v) {
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
-        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-    }
-    return v;
-}
-
-// Offset of this lane's 16 bytes of group gl of row g inside a slot's codes
-// (row g + 8 is the same offset in the second box): the TMA box's 128-byte
-// swizzle XORs the 16-byte unit index with the row's index inside the
-// 1024-byte swizzle atom.
-__device__ __forceinline__ uint32_t a_offset(int gl, int g, int t) {
-    const int ell = gl >> 1;
-    const uint32_t phys = (uint32_t)((((gl & 1) << 2) | t) ^ (((g & 1) << 2) | ell));
-    return (uint32_t)(g * 512 + ell * 128) + (phys << 4);
-}
-
-// The group's 8 MMAs and its epilogue into acc.  wa, wb: this lane's packed
-// words of rows g and g + 8; s0, z0, s1, z1: the two rows' scale and zero;
-// bg: staged B row address of this lane's column at the group (loaded only
-// where bact is set: B columns without a token are zero); c0, c1: C1/C2
-// addresses of columns 2t and 2t + 1 at the group.
-__device__ __forceinline__ void compute_group(float (&acc)[4], uint4 wa, uint4 wb, float s0, float z0, float s1,
-                                              float z1, int t, uint32_t bg, uint32_t bact, uint32_t c0, uint32_t c1) {
-    uint4 b[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) b[i] = lds128_if(bg + ((uint32_t)stage_word(4 * t + i) << 4), bact);
-    const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w};
-    const uint32_t Bw[4] = {wb.x, wb.y, wb.z, wb.w};
-    float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t x = A[i], y = Bw[i];
-        const uint32_t xs = x >> 8, ys = y >> 8;
-        const uint32_t a0 = lop_mask_or(x, 0x000F000Fu, 0x64006400u);   // (q0, q4) + 1024
-        const uint32_t a2 = lop_mask_or(x, 0x00F000F0u, 0x54005400u);   // (q1, q5) + 64
-        const uint32_t a1 = lop_mask_or(y, 0x000F000Fu, 0x64006400u);
-        const uint32_t a3 = lop_mask_or(y, 0x00F000F0u, 0x54005400u);
-        mma16816(da, a0, a1, a2, a3, b[i].x, b[i].y);
-        const uint32_t e0 = lop_mask_or(xs, 0x000F000Fu, 0x64006400u);  // (q2, q6) + 1024
-        const uint32_t e2 = lop_mask_or(xs, 0x00F000F0u, 0x54005400u);  // (q3, q7) + 64
-        const uint32_t e1 = lop_mask_or(ys, 0x000F000Fu, 0x64006400u);
-        const uint32_t e3 = lop_mask_or(ys, 0x00F000F0u, 0x54005400u);
-        mma16816(db, e0, e1, e2, e3, b[i].z, b[i].w);
-    }
-    const float2 ca = lds_f2(c0), cb = lds_f2(c1);
-    acc[0] = fmaf(s0, (da[0] + db[0]) - fmaf(z0, ca.y, ca.x), acc[0]);
-    acc[1] = fmaf(s0, (da[1] + db[1]) - fmaf(z0, cb.y, cb.x), acc[1]);
-    acc[2] = fmaf(s1, (da[2] + db[2]) - fmaf(z1, ca.y, ca.x), acc[2]);
-    acc[3] = fmaf(s1, (da[3] + db[3]) - fmaf(z1, cb.y, cb.x), acc[3]);
-}
-
-__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFFu))); }
-__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
 
 // This warp's NG groups (gb .. gb + NG - 1 of the chunk whose codes are at sa
 // and whose scales and zeros are at szs): the scales and zeros are copied
@@ -398,20 +164,41 @@ __device__ __forceinline__ void consume_groups(float (&acc)[4], uint32_t sa, uin
                 sz[a][w] = lo | (hi << 16);
             }
     }
+    // groups in pairs (two groups' MMAs interleaved: four independent
+    // chains), each pair's codes loaded right before its math; the slot is
+    // given back after the last codes are loaded
 #pragma unroll
-    for (int i = 0; i < NG; ++i) {
-        const uint32_t aoff = a_offset(gb + i, g, t);
-        const uint4 wai = lds128(sa + aoff), wbi = lds128(sa + BOX_BYTES + aoff);
-        if (i == NG - 1) {
+    for (int i = 0; i < NG; i += 2) {
+        const bool two = i + 1 < NG;
+        const uint32_t aoff0 = a_offset(gb + i, g, t);
+        const uint4 wa0 = lds128(sa + aoff0), wb0 = lds128(sa + BOX_BYTES + aoff0);
+        uint4 wa1 = wa0, wb1 = wb0;
+        if (two) {
+            const uint32_t aoff1 = a_offset(gb + i + 1, g, t);
+            wa1 = lds128(sa + aoff1);
+            wb1 = lds128(sa + BOX_BYTES + aoff1);
+        }
+        if (i + 2 >= NG) {
             __syncwarp();
             if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty);
         }
         const uint32_t gi = (uint32_t)(gi0 + gb + i);
-        float v[4];
+        float v0[4], v1[4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) v[a] = (i & 1) ? half_hi(sz[a][i >> 1]) : half_lo(sz[a][i >> 1]);
-        compute_group(acc, wai, wbi, v[0] * wscale, v[1], v[2] * wscale, v[3], t, brow_a + 256u * gi, bact,
-                      c0_a + 8u * gi, c1_a + 8u * gi);
+        for (int a = 0; a < 4; ++a) {
+            v0[a] = (i & 1) ? half_hi(sz[a][i >> 1]) : half_lo(sz[a][i >> 1]);
+            v1[a] = ((i + 1) & 1) ? half_hi(sz[a][(i + 1) >> 1]) : half_lo(sz[a][(i + 1) >> 1]);
+        }
+        v0[0] *= wscale;
+        v0[2] *= wscale;
+        v1[0] *= wscale;
+        v1[2] *= wscale;
+        if (two)
+            compute_group2(acc, wa0, wb0, wa1, wb1, v0, v1, t, brow_a + 256u * gi, brow_a + 256u * (gi + 1), bact,
+                           c0_a + 8u * gi, c1_a + 8u * gi, c0_a + 8u * (gi + 1), c1_a + 8u * (gi + 1));
+        else
+            compute_group(acc, wa0, wb0, v0[0], v0[1], v0[2], v0[3], t, brow_a + 256u * gi, bact, c0_a + 8u * gi,
+                          c1_a + 8u * gi);
     }
 }
 
@@ -461,14 +248,10 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     const int nslot = p.nslot, ns4 = nslot / NQ;
 
     // ------------------------------------------------ phase 0: init, routing
-    // Scratch of phase 0 lives in the ring, which is idle until the producers
-    // start: the routed tokens' logits, then per-expert counts of the first and
-    // second 32 assignments and the touched-expert bitmask.
+    // The routed tokens' logits live in the ring, which is idle until the
+    // producers start.
     float* lgs = reinterpret_cast<float*>(sm);
-    int32_t* cnt_a = reinterpret_cast<int32_t*>(sm + p.off_cnt);
-    int32_t* cnt_b = cnt_a + E;
-    uint32_t* emask = reinterpret_cast<uint32_t*>(cnt_b + E);
-    int32_t* wpre = reinterpret_cast<int32_t*>(emask + 32);
+    const int nsort = T > 2 ? T : 2;  // warps that route (t < T) and sort (warps 0, 1)
     if (threadIdx.x == 0) tab.abort = 0;
     if (warp == PRODUCER_WARP) {
         for (int i = lane; i < NQ * NFQ; i += 32) tc::mbar_init(full0 + 8u * i, FULL_ARRIVALS);
@@ -486,11 +269,6 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
                 tc::tma_prefetch_desc(&map2z);
             }
         }
-    } else if (warp == 0) {
-        // the sort's counters (warp 0 sorts right after routing, see below)
-        for (int i = lane; i < 2 * E; i += 32) cnt_a[i] = 0;
-        emask[lane] = 0;
-        __syncwarp();
     }
     // Launched as a programmatic dependent of the previous kernel on the
     // stream (when the driver accepts it), the CTA may start while that kernel
@@ -499,91 +277,61 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     // so wait until the previous grid has completed and its writes are
     // visible.  (Without a programmatic dependency this returns at once.)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (warp < T) {
-        // this token's logits into shared memory, then top-k
-        float* lrow = lgs + warp * E;
-        const float* src = p.logits + (size_t)warp * E;
-        for (int e = lane; e < E; e += 32) lrow[e] = __ldg(src + e);
-        __syncwarp();
-        route_token(lrow, E, k, &tab.ids[warp * k], &tab.w[warp * k]);
-        // every token routed: warp 0 sorts while the other warps still stage
-        // the activations
-        bar_sync(15, 32 * T);
-        if (warp == 0) {
-            // stable counting sort of the R <= 64 assignments by expert: per-expert
-            // counts of the two halves, the touched-expert bitmask (ascending expert
-            // list by a warp scan), ranks inside an expert from __match_any_sync
-            const int a0 = lane, a1 = lane + 32;
-            const bool v0 = a0 < R, v1 = a1 < R;
-            const int e0 = v0 ? tab.ids[a0] : 0, e1 = v1 ? tab.ids[a1] : 0;
-            if (v0) {
-                atomicAdd(&cnt_a[e0], 1);
-                atomicOr(&emask[e0 >> 5], 1u << (e0 & 31));
-            }
-            if (v1) {
-                atomicAdd(&cnt_b[e1], 1);
-                atomicOr(&emask[e1 >> 5], 1u << (e1 & 31));
-            }
-            const uint32_t m0 = __match_any_sync(0xffffffffu, v0 ? e0 : -1 - lane);
-            const uint32_t m1 = __match_any_sync(0xffffffffu, v1 ? e1 : -1 - lane);
-            const uint32_t lt = (1u << lane) - 1u;
+    if (warp < nsort) {
+        if (warp < T) {
+            // this token's logits into shared memory, then top-k
+            float* lrow = lgs + warp * E;
+            const float* src = p.logits + (size_t)warp * E;
+            for (int e = lane; e < E; e += 32) lrow[e] = __ldg(src + e);
             __syncwarp();
-            // ascending expert list: lane l owns bitmask word l
-            const uint32_t w = emask[lane];
-            int incl = __popc(w);
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
+            route_token(lrow, E, k, &tab.ids[warp * k], &tab.w[warp * k]);
+            // the logits' ring bytes are overwritten by TMA once the producers start
+            tc::fence_proxy_async_smem();
+        }
+        // every token routed: warps 0 and 1 sort while the other warps still
+        // stage the activations
+        bar_sync(15, 32 * nsort);
+        if (warp < 2) {
+            // Stable counting sort of the R <= 64 assignments by expert, one
+            // thread per assignment a: its position is the number of
+            // assignments with a smaller expert plus those of the same expert
+            // before it; its expert's index in the ascending list of touched
+            // experts is the number of distinct smaller experts.
+            const int a = threadIdx.x;
+            const bool va = a < R;
+            const int ea = va ? tab.ids[a] : INT_MAX;
+            int lt = 0, eqb = 0, eqall = 0;
+            for (int b = 0; b < R; ++b) {
+                const int eb = tab.ids[b];
+                lt += eb < ea;
+                eqall += eb == ea;
+                eqb += (eb == ea) & (b < a);
             }
-            const int U = __shfl_sync(0xffffffffu, incl, 31);
-            int pre = incl - __popc(w);
-            wpre[lane] = pre;
-            for (uint32_t b = w; b; b &= b - 1) tab.uexp[pre++] = 32 * lane + (__ffs(b) - 1);
-            __syncwarp();
-            // expert counts and offsets in list order (U <= 64)
-            const int c0 = lane < U ? cnt_a[tab.uexp[lane]] + cnt_b[tab.uexp[lane]] : 0;
-            const int c1 = lane + 32 < U ? cnt_a[tab.uexp[lane + 32]] + cnt_b[tab.uexp[lane + 32]] : 0;
-            int s0 = c0, s1 = c1;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y0 = __shfl_up_sync(0xffffffffu, s0, o);
-                const int y1 = __shfl_up_sync(0xffffffffu, s1, o);
-                if (lane >= o) {
-                    s0 += y0;
-                    s1 += y1;
-                }
+            const int first = (va && eqb == 0) ? 1 : 0;
+            tab.first[a] = first;
+            bar_sync(14, 64);
+            int ui = 0, nu = 0;
+            for (int b = 0; b < R; ++b) {
+                const int fb = tab.first[b];
+                nu += fb;
+                ui += fb & (tab.ids[b] < ea);
             }
-            const int tot0 = __shfl_sync(0xffffffffu, s0, 31);
-            if (lane < U) {
-                tab.ucnt[lane] = c0;
-                tab.uoff[lane] = s0 - c0;
+            if (va) {
+                const int pos = lt + eqb;
+                tab.pos[a] = pos;
+                tab.ptok[pos] = (int)fd_div((uint32_t)a, p.fd_k);
             }
-            if (lane + 32 < U) {
-                tab.ucnt[lane + 32] = c1;
-                tab.uoff[lane + 32] = tot0 + s1 - c1;
+            if (first) {
+                tab.uexp[ui] = ea;
+                tab.uoff[ui] = lt;
+                tab.ucnt[ui] = eqall;
             }
-            __syncwarp();
-            // permuted position of each assignment
-            auto uidx = [&](int e) {
-                return wpre[e >> 5] + __popc(emask[e >> 5] & ((1u << (e & 31)) - 1u));
-            };
-            if (v0) {
-                const int pos = tab.uoff[uidx(e0)] + __popc(m0 & lt);
-                tab.pos[a0] = pos;
-                tab.ptok[pos] = (int)fd_div((uint32_t)a0, p.fd_k);
-            }
-            if (v1) {
-                const int pos = tab.uoff[uidx(e1)] + cnt_a[e1] + __popc(m1 & lt);
-                tab.pos[a1] = pos;
-                tab.ptok[pos] = (int)fd_div((uint32_t)a1, p.fd_k);
-            }
-            if (lane == 0) tab.n_uniq = U;
+            if (a == 0) tab.n_uniq = nu;
         }
     } else if (warp < CW) {
         // activations -> fp16 in MMA order, plus C1/C2 per (token, group); the
         // C1/C2 row T is zero (B columns without a token)
-        const int nthr = (CW - T) * 32, tid = (warp - T) * 32 + lane;
+        const int nthr = (CW - nsort) * 32, tid = (warp - nsort) * 32 + lane;
         const int wpr = d >> 3;  // 16-byte words per row (a multiple of 32)
         float2* cx = reinterpret_cast<float2*>(sm + p.off_cx);
         for (int wi = tid; wi < T * wpr; wi += nthr) {
@@ -1074,7 +822,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
 struct Layout {
     int nslot;
     size_t smem;
-    uint32_t off_sz, off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab, off_cnt;
+    uint32_t off_sz, off_bars, off_xb, off_cx, off_hs, off_ch, off_red, off_red2, off_tab;
     int xb_stride, hs_stride;
 };
 
@@ -1116,9 +864,8 @@ bool plan_layout(int T, int k, int E, int d, int f, int G, int nq, Layout* L) {
     // two slots per pipeline at least (a consumer's slot index advances by at
     // most 2 per chunk), and the full-barrier bound NFQ >= slots + 3
     if (nslot < 2 * NQ || nslot / NQ + 3 > NFQ) return false;
-    // phase-0 scratch in the ring: logits, two count arrays, bitmask, word prefixes
-    l.off_cnt = (uint32_t)align_up((size_t)T * E * 4, 16);
-    if (l.off_cnt + (size_t)8 * E + 256 > (size_t)nslot * SLOT_CODE) return false;
+    // phase-0 scratch in the ring: the routed tokens' logits
+    if ((size_t)T * E * 4 > (size_t)nslot * SLOT_CODE) return false;  // routing scratch in the ring
     const uint32_t ring = (uint32_t)nslot * SLOT_CODE;
     const uint32_t szs = (uint32_t)nslot * SLOT_SZ;
     const uint32_t base = ring + szs + (uint32_t)bar_fixed;
@@ -1217,7 +964,6 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     p.off_red = l.off_red;
     p.off_red2 = l.off_red2;
     p.off_tab = l.off_tab;
-    p.off_cnt = l.off_cnt;
     p.xb_stride = l.xb_stride;
     p.hs_stride = l.hs_stride;
     const bool bulk13 = Gd < CHUNK_GROUPS && a16(W.w13_s) && a16(W.w13_z);

@@ -40,7 +40,10 @@ struct AlignOut {
     uint32_t* err;
 };
 constexpr int ALIGN_SMALL_MAX_R = 2048;   // single-CTA permutation up to this many rows
-constexpr int ALIGN_BLOCK_ROWS = 1024;    // assignments per CTA on the multi-block path
+constexpr int ALIGN_BLOCK_ROWS = 1024;    // most assignments per CTA on the multi-block path
+// Assignments per CTA on the multi-block path: 256 (more CTAs for the stable
+// scatter) while the per-block count table stays within 64 KB, else 1024.
+int align_block_rows(int R, int E);
 size_t align_blockcnt_bytes(int R, int E);
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, const uint16_t* x, int d,
                          const AlignOut& o, cudaStream_t s);
@@ -96,10 +99,17 @@ struct FusedIn {
     uint16_t* out;           // bf16 [T][d]
     int32_t* ids_out;        // [T][k] or null
     uint16_t* hb;            // fp16 scratch, [T*k][f]
-    void* ws;                // workspace (header: error word and grid-barrier counter)
+    float* ybuf;             // fp32 scratch, [T*k][d] (dataflow kernel)
+    void* ws;                // workspace (header: error word and the kernels' counters)
 };
 bool decode_fused_supported(int T, int k, int E, int d, int f);
 cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s);
+// The same layer as a dataflow kernel without a grid barrier (decode_flow.cu).
+// Its counters take flow_counter_bytes(T, d) bytes right after the workspace
+// header.
+bool decode_flow_supported(int T, int k, int E, int d, int f);
+cudaError_t launch_decode_flow(const FusedIn& in, cudaStream_t s);
+size_t flow_counter_bytes(int T, int d);
 
 // ---------------------------------------------- prefill regime (tcgen05)
 struct TcIn {

@@ -138,12 +138,23 @@ __device__ void gather_rows(const uint16_t* __restrict__ x, int d, int k, const 
         if (a < 0 || a >= i1) continue;  // a slot left unwritten by out-of-range ids
         const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(a / k) * d);
         uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)i * d);
-        for (int v = lane; v < vec; v += 32) {
-            uint4 q = src[v];
-            if (TO_F16)
-                q = k8_interleave(bf16x2_to_f16x2(q.x, bad), bf16x2_to_f16x2(q.y, bad), bf16x2_to_f16x2(q.z, bad),
-                                  bf16x2_to_f16x2(q.w, bad));
-            dst[v] = q;
+        // 8 vectors per lane at a time, all loads in flight before the stores
+        for (int v0 = 0; v0 < vec; v0 += 256) {
+            uint4 q[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + lane + 32 * u;
+                if (v < vec) q[u] = src[v];
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + lane + 32 * u;
+                if (v >= vec) break;
+                if (TO_F16)
+                    q[u] = k8_interleave(bf16x2_to_f16x2(q[u].x, bad), bf16x2_to_f16x2(q[u].y, bad),
+                                         bf16x2_to_f16x2(q[u].z, bad), bf16x2_to_f16x2(q[u].w, bad));
+                dst[v] = q[u];
+            }
         }
     }
     if (TO_F16 && bad) set_error(err, ERRBIT_F16_RANGE);
@@ -183,13 +194,13 @@ __global__ void __launch_bounds__(SCAN_THREADS) align_small_kernel(const int32_t
 }
 
 // -------------------------------------------------------- multi-block path
-__global__ void __launch_bounds__(256) align_hist_kernel(const int32_t* __restrict__ ids, int R, int E,
+__global__ void __launch_bounds__(256) align_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int rows,
                                                          int32_t* __restrict__ blockcnt, uint32_t* err) {
     __shared__ int cnt[1024];
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
-    const int a0 = blockIdx.x * ALIGN_BLOCK_ROWS;
-    const int a1 = min(R, a0 + ALIGN_BLOCK_ROWS);
+    const int a0 = blockIdx.x * rows;
+    const int a1 = min(R, a0 + rows);
     for (int a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
         const int e = ids[a];
         if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
@@ -227,12 +238,12 @@ __global__ void __launch_bounds__(SCAN_THREADS) align_scan_kernel(int nblocks, i
 
 // One warp per block of assignments: the block's ids are first copied to
 // shared memory with all loads in flight at once, then placed in order.
-__global__ void __launch_bounds__(32) align_scatter_kernel(const int32_t* __restrict__ ids, int R, int E,
+__global__ void __launch_bounds__(32) align_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int rows,
                                                            const int32_t* __restrict__ blockcnt, AlignOut o) {
     __shared__ int run[1024];
     __shared__ int32_t bid[ALIGN_BLOCK_ROWS];
-    const int a0 = blockIdx.x * ALIGN_BLOCK_ROWS;
-    const int a1 = min(R, a0 + ALIGN_BLOCK_ROWS);
+    const int a0 = blockIdx.x * rows;
+    const int a1 = min(R, a0 + rows);
     for (int e = threadIdx.x; e < E; e += 32) run[e] = blockcnt[(size_t)blockIdx.x * E + e];
     for (int a = a0 + threadIdx.x; a < a1; a += 32) bid[a - a0] = ids[a];
     __syncwarp();
@@ -264,9 +275,13 @@ __global__ void __launch_bounds__(SCAN_THREADS) plan_from_offsets_kernel(const i
 
 }  // namespace
 
+int align_block_rows(int R, int E) {
+    return (size_t)ceil_div(R, 256) * E * sizeof(int32_t) <= 65536 ? 256 : ALIGN_BLOCK_ROWS;
+}
+
 size_t align_blockcnt_bytes(int R, int E) {
     if (R <= ALIGN_SMALL_MAX_R) return 0;
-    return (size_t)ceil_div(R, ALIGN_BLOCK_ROWS) * E * sizeof(int32_t);
+    return (size_t)ceil_div(R, align_block_rows(R, E)) * E * sizeof(int32_t);
 }
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, const uint16_t* x, int d,
@@ -277,12 +292,13 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, const uint16_t
         note_launch();
         return cudaGetLastError();
     }
-    const int nb = ceil_div(R, ALIGN_BLOCK_ROWS);
-    align_hist_kernel<<<nb, 256, 0, s>>>(ids, R, E, o.blockcnt, o.err);
+    const int rows = align_block_rows(R, E);
+    const int nb = ceil_div(R, rows);
+    align_hist_kernel<<<nb, 256, 0, s>>>(ids, R, E, rows, o.blockcnt, o.err);
     note_launch();
     align_scan_kernel<<<1, SCAN_THREADS, 0, s>>>(nb, E, o.blockcnt, o);
     note_launch();
-    align_scatter_kernel<<<nb, 32, 0, s>>>(ids, R, E, o.blockcnt, o);
+    align_scatter_kernel<<<nb, 32, 0, s>>>(ids, R, E, rows, o.blockcnt, o);
     note_launch();
     if (o.x_perm) {
         const int blocks = min(ceil_div(R, 8), 8 * num_sms());

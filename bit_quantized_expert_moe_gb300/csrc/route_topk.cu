@@ -5,14 +5,28 @@
 // arg-max whose tie rule is "lower expert id wins"; the comparisons are exact
 // on the fp32 values, so the ids are exactly those of a sort by
 // (-logit, id) (router ids must match exactly: "Performance and
-// verification", section "How it is verified").
+// verification", section "How it is verified").  For k <= 64 the selected
+// values stay in registers (route_topk_regs_kernel); larger k keeps them in
+// the output arrays between rounds.
 #include <cfloat>
 #include <climits>
 
+#include "decode_ops.cuh"
 #include "internal.h"
 
 namespace moe {
 namespace {
+
+// k <= 64: the selection in registers (order-preserving uint32 keys, k rounds
+// of warp max and lowest id among the lanes holding it; lane j keeps slot j
+// and j + 32) with one store of the ids and weights at the end.
+template <int VPL>
+__global__ void __launch_bounds__(256) route_topk_regs_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                              int32_t* __restrict__ ids, float* __restrict__ w) {
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    dec::route_token_regs<VPL>(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
+}
 
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
     return (v > bv) || (v == bv && e < be);
@@ -82,7 +96,10 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 template <int VPL>
 cudaError_t launch_vpl(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
     const int warps = 8;
-    route_topk_kernel<VPL><<<ceil_div(T, warps), warps * 32, 0, s>>>(logits, T, E, k, ids, w);
+    if (k <= 64)
+        route_topk_regs_kernel<VPL><<<ceil_div(T, warps), warps * 32, 0, s>>>(logits, T, E, k, ids, w);
+    else
+        route_topk_kernel<VPL><<<ceil_div(T, warps), warps * 32, 0, s>>>(logits, T, E, k, ids, w);
     note_launch();
     return cudaGetLastError();
 }

@@ -60,6 +60,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
+// The same with a short suspend hint, for a waiter that has other work to
+// look at between tries.
+constexpr uint32_t WAIT_SUSPEND_SHORT_NS = 500;
+__device__ __forceinline__ bool mbar_try_wait_sleep_short(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(WAIT_SUSPEND_SHORT_NS) : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of parity `parity` to complete.  On timeout it
 // records ERRBIT_TIMEOUT, raises the CTA abort flag and returns false; a wait
 // that sees the abort flag raised by another role returns false soon after.
