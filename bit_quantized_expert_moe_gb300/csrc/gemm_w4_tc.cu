@@ -4,13 +4,19 @@
 // "Performance and verification", section "Why it is fast": a prompt's
 // expert products are batched into grouped tensor-core GEMMs; "Measured
 // results", section Speed: prompts run fastest with the 4-bit weights widened
-// to 16-bit for a dense GEMM.  Here the dequantisation happens tile by tile in shared
-// memory, never in HBM.
+// to 16-bit for a dense GEMM.  Here the dequantisation happens tile by tile on
+// chip, never in HBM: the widened weights go from registers straight into
+// tensor memory, where the MMA reads its A operand.
 //
 // Shapes (swap-AB: weight rows are the MMA's M, tokens its N):
 //   D[m][n] = sum_k A[m][k] * B[n][k]     M = 128 weight rows, N <= 256 tokens
-//   A = dequantised weights (fp16, written by the dequant warps, SW128 K-major)
+//   A = dequantised weights (fp16, written by the dequant warps into tensor
+//       memory: lane = row, a 32-bit column = two consecutive K elements)
 //   B = activation rows of one expert segment (fp16, TMA, SW128 K-major)
+// Shared memory then carries only B, the packed codes and the scales: per
+// 64-K stage the MMA reads 32 KB of B and TMA writes 36 KB, against 104 KB of
+// traffic with A staged in shared memory (written 16 KB, read 16 KB), which
+// bounded the stage time.
 // The operands are fp16 rather than bf16: bf16 activations convert to fp16
 // exactly inside fp16's range (values outside set the error word), and a
 // weight is q s - fl16(z s) rounded once to fp16, which keeps 3 more bits than
@@ -26,8 +32,14 @@
 // down: 128 consecutive rows of W2; the epilogue writes y rows (fp16 for the
 // layer's own combine, bf16 when y is the caller's output).
 //
-// Warp roles (512 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
-// 2-3 idle, 4-11 dequantisation, 12-15 epilogue (TMEM lane quarters 0..3).
+// Warp roles (640 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
+// 2-3 idle, 4-11 dequantisation (warp w: TMEM lane quarter w % 4, half
+// (w - 4) / 4 of a stage's K), 12-19 epilogue (warp w: lane quarter w % 4,
+// every other 32-column block).  With one accumulator the next item's MMAs
+// wait until the epilogue has read it, so two warps per quarter halve that
+// wait.
+// TMEM: the fp32 accumulator in columns 0..255, stage s's A in columns
+// 256 + 32 s .. + 31.
 // Every wait is bounded in time; a timeout sets the error word, every role
 // leaves its loop, in-flight copies and MMAs are drained, TMEM is freed.
 #include <cstdio>
@@ -41,16 +53,17 @@ namespace {
 constexpr int BM = 128;                  // A rows per item
 constexpr int BK = 64;                   // K per stage: one 128-byte swizzle row of fp16
 constexpr int BN = TILE_ROWS;            // max tokens per item (256)
-constexpr int A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_BYTES = BN * BK * 2;     // 32 KB
 constexpr int P_BYTES = BM * BK / 2;     // 4 KB of packed codes
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + P_BYTES;
+constexpr int STAGE_BYTES = B_BYTES + P_BYTES;
 constexpr int B_BOX_ROWS = 64;           // activation rows per TMA box (fewer, larger copies: the single producer thread issues every one)
 constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
-constexpr int THREADS = 512;
+constexpr int THREADS = 640;
 constexpr int DQ_WARP0 = 4, DQ_WARPS = 8;
-constexpr int EP_WARP0 = 12;
-constexpr uint32_t TMEM_COLS = 512;      // two accumulators of 256 fp32 columns
+constexpr int EP_WARP0 = 12, EP_WARPS = 8;
+constexpr uint32_t TMEM_COLS = 512;      // accumulator (256 columns) + S <= 6 A stages of 32 columns
+constexpr uint32_t A_COL0 = 256;         // first TMEM column of stage 0's A
+constexpr uint32_t A_STAGE_COLS = BK / 2;
 
 struct TcParams {
     int E, d, f, R;
@@ -124,14 +137,14 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* gbase = smem_raw + (base - raw);
 
-    const uint32_t sA = base;
-    const uint32_t sB = base + S * A_BYTES;
-    const uint32_t sP = base + S * (A_BYTES + B_BYTES);
+    const uint32_t sB = base;
+    const uint32_t sP = base + S * B_BYTES;
     const int G = p.K / 128;
     uint16_t* sScale = reinterpret_cast<uint16_t*>(gbase + S * STAGE_BYTES);  // [2][BM][G]
     uint16_t* sZero = sScale + 2 * BM * G;                                     // [2][BM][G]
     const uint32_t bars = base + S * STAGE_BYTES + (uint32_t)scale_bytes(p.K);
     // barrier layout: full[S], afull[S], empty[S], accfull[2], accempty[2], done
+    // (one accumulator: only accfull[0] and accempty[0] are used)
     const uint32_t bar_full = bars, bar_afull = bars + 8 * S, bar_empty = bars + 16 * S;
     const uint32_t bar_accfull = bars + 24 * S, bar_accempty = bar_accfull + 16, bar_done = bar_accempty + 16;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + S * STAGE_BYTES + scale_bytes(p.K) + 8 * (3 * S + 5));
@@ -149,7 +162,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(bar_accfull + 8 * b, 1);
-            tc::mbar_init(bar_accempty + 8 * b, 4);
+            tc::mbar_init(bar_accempty + 8 * b, EP_WARPS);
         }
         tc::mbar_init(bar_done, 1);
         *abort_flag = 0;
@@ -213,27 +226,26 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 item_rows<GATEUP>(p, item, e, row0, nrows, fb);
                 const int N = ceil_div(nrows, 16) * 16;
                 const uint32_t idesc = tc::idesc_f16_f32(BM, N);
-                const int buf = ic & 1;
-                const uint32_t aph = (ic >> 1) & 1;
-                if (!tc::mbar_wait(bar_accempty + 8 * buf, aph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                const uint32_t aph = ic & 1;
+                if (!tc::mbar_wait(bar_accempty, aph ^ 1, abort_flag, p.err)) { ok = false; break; }
                 tc::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * 256;
+                const uint32_t d_tmem = tmem_base;
                 for (int kc = 0; kc < NK; ++kc) {
                     if (!tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err) ||
                         !tc::mbar_wait(bar_afull + 8 * stage, phase, abort_flag, p.err)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t a0 = sA + stage * A_BYTES, b0 = sB + stage * B_BYTES;
+                    const uint32_t a0 = tmem_base + A_COL0 + A_STAGE_COLS * stage, b0 = sB + stage * B_BYTES;
 #pragma unroll
                     for (int ks = 0; ks < BK / 16; ++ks) {
-                        tc::mma_f16(d_tmem, tc::sw128_kmajor_desc(a0 + ks * 32), tc::sw128_kmajor_desc(b0 + ks * 32),
-                                     idesc, (kc | ks) != 0);
+                        tc::mma_f16_tmem_a(d_tmem, a0 + 8 * ks, tc::sw128_kmajor_desc(b0 + ks * 32), idesc,
+                                           (kc | ks) != 0);
                     }
                     tc::mma_commit(bar_empty + 8 * stage);
                     any = true;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                tc::mma_commit(bar_accfull + 8 * buf);
+                tc::mma_commit(bar_accfull);
             }
             // drain: all issued MMAs complete before TMEM is released
             if (any) {
@@ -243,21 +255,25 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         }
     } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + DQ_WARPS) {
         // ------------------------------------------------------ dequantisers
-        // Warp dw owns A rows dw*16 .. dw*16+15 of every stage; it prefetches
-        // those rows' scales and zeros itself (4-byte cp.async), so only warp-
-        // level synchronisation is needed.  Waits are made warp-uniform.
-        const int dt = threadIdx.x - DQ_WARP0 * 32;
-        const int dw = dt >> 5;
-        const int w = lane & 7;
+        // Warp w owns A row r = 32 (w % 4) + lane (its TMEM lane) and half
+        // hk = (w - 4) / 4 of every stage's K: 4 packed words (32 codes) per
+        // stage, widened in registers and stored as 16 TMEM columns.  Each
+        // warp prefetches the scales and zeros of the rows it reads (4-byte
+        // cp.async; the two warps of a lane quarter copy the same values), so
+        // only warp-level synchronisation is needed.  Waits are warp-uniform.
+        const int q = warp & 3, hk = (warp - DQ_WARP0) >> 2;
+        const int r = 32 * q + lane;
+        const int prow = a_packed_row<GATEUP>(r);
+        const uint32_t t_lane = (uint32_t)(32 * q) << 16;
         auto prefetch_scales = [&](int item, int buf) {
             int e, row0, nrows, fb;
             item_rows<GATEUP>(p, item, e, row0, nrows, fb);
             const int pairs = G / 2;
-            for (int idx = lane; idx < 16 * pairs; idx += 32) {
-                const int r = dw * 16 + idx / pairs, gp = idx % pairs;
-                const size_t grow = a_global_row<GATEUP>(p, e, fb, r);
+            for (int idx = lane; idx < 32 * pairs; idx += 32) {
+                const int rr = 32 * q + idx / pairs, gp = idx % pairs;
+                const size_t grow = a_global_row<GATEUP>(p, e, fb, rr);
                 const size_t src = grow * G + 2 * gp;
-                const size_t dst = ((size_t)buf * BM + r) * G + 2 * gp;
+                const size_t dst = ((size_t)buf * BM + rr) * G + 2 * gp;
                 cp_async4(smem_u32(sScale + dst), p.wsc + src);
                 cp_async4(smem_u32(sZero + dst), p.wz + src);
             }
@@ -275,53 +291,38 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             cp_async_commit();
             cp_async_wait<1>();
             __syncwarp();  // this item's scales visible to the whole warp
-            int r_it[4], prow[4];
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                r_it[it] = dw * 16 + it * 4 + (lane >> 3);
-                prow[it] = a_packed_row<GATEUP>(r_it[it]);
-            }
-            uint32_t s2[4], nzs2[4];  // per row, as f16x2: (s, s) and (-fl16(z s), -fl16(z s))
+            uint32_t s2 = 0, nzs2 = 0;  // as f16x2: (s, s) and (-fl16(z s), -fl16(z s))
             for (int kc = 0; kc < NK; ++kc) {
                 ok = tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 if ((kc & 1) == 0) {
-                    const int g = kc >> 1;
-#pragma unroll
-                    for (int it = 0; it < 4; ++it) {
-                        const size_t si = ((size_t)sbuf * BM + r_it[it]) * G + g;
-                        const uint32_t sb = sScale[si];
-                        const float zs = half_bits_to_float((uint16_t)sb) * half_bits_to_float(sZero[si]);
-                        s2[it] = sb * 0x10001u;
-                        nzs2[it] = (uint32_t)float_to_f16_bits(-zs) * 0x10001u;
-                    }
+                    const size_t si = ((size_t)sbuf * BM + r) * G + (kc >> 1);
+                    const uint32_t sb = sScale[si];
+                    const float zs = half_bits_to_float((uint16_t)sb) * half_bits_to_float(sZero[si]);
+                    s2 = sb * 0x10001u;
+                    nzs2 = (uint32_t)float_to_f16_bits(-zs) * 0x10001u;
                 }
-                const uint32_t* pk = reinterpret_cast<const uint32_t*>(gbase + (sP - base) + stage * P_BYTES);
-                const uint32_t a0 = sA + stage * A_BYTES;
+                // this row's 4 words of the half: codes 32 hk .. 32 hk + 31 of the stage
+                const uint4 pw = *reinterpret_cast<const uint4*>(gbase + (sP - base) + stage * P_BYTES + prow * 32 + hk * 16);
+                const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
+                uint32_t o[16];
 #pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    // the 8 codes of one word in the operand order (k0,k4) (k1,k5)
-                    // (k2,k6) (k3,k7): masking a nibble into the mantissa of
-                    // 1024.0 (bits 0-3) or 64.0 (bits 4-7) gives 1024 + q or
-                    // 64 + q exactly, minus the base gives q exactly, and one
-                    // fma gives q s - fl16(z s) rounded once
-                    const uint32_t word = pk[prow[it] * 8 + w];
-                    const uint32_t ws = word >> 8;
-                    const uint32_t o0 = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x000F000Fu, 0x64006400u), 0x64006400u),
-                                                  s2[it], nzs2[it]);
-                    const uint32_t o1 = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x00F000F0u, 0x54005400u), 0x54005400u),
-                                                  s2[it], nzs2[it]);
-                    const uint32_t o2 = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x000F000Fu, 0x64006400u), 0x64006400u),
-                                                  s2[it], nzs2[it]);
-                    const uint32_t o3 = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x00F000F0u, 0x54005400u), 0x54005400u),
-                                                  s2[it], nzs2[it]);
-                    const int r = r_it[it];
-                    const uint32_t dst = a0 + (r >> 3) * 1024 + (r & 7) * 128 + ((w ^ (r & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
-                                 :: "r"(dst), "r"(o0), "r"(o1), "r"(o2), "r"(o3) : "memory");
+                for (int wi = 0; wi < 4; ++wi) {
+                    // the 8 codes of one word in the operand order (k0,k4)
+                    // (k1,k5) (k2,k6) (k3,k7): masking a nibble into the
+                    // mantissa of 1024.0 (bits 0-3) or 64.0 (bits 4-7) gives
+                    // 1024 + q or 64 + q exactly, minus the base gives q
+                    // exactly, and one fma gives q s - fl16(z s) rounded once
+                    const uint32_t word = words[wi], ws = word >> 8;
+                    o[4 * wi + 0] = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x000F000Fu, 0x64006400u), 0x64006400u), s2, nzs2);
+                    o[4 * wi + 1] = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x00F000F0u, 0x54005400u), 0x54005400u), s2, nzs2);
+                    o[4 * wi + 2] = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x000F000Fu, 0x64006400u), 0x64006400u), s2, nzs2);
+                    o[4 * wi + 3] = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x00F000F0u, 0x54005400u), 0x54005400u), s2, nzs2);
                 }
-                tc::fence_proxy_async_smem();
+                tc::tmem_st_32x32b_x16(tmem_base + t_lane + A_COL0 + A_STAGE_COLS * stage + 16 * hk, o);
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar_afull + 8 * stage);
                 if (++stage == S) { stage = 0; phase ^= 1; }
@@ -330,21 +331,28 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         cp_async_wait<0>();
     } else if (warp >= EP_WARP0) {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quarter
+        const int q = warp & 3;                 // TMEM lane quarter
+        const int eh = (warp - EP_WARP0) >> 2;  // column blocks eh, eh + 2, ...
         int ic = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ic) {
             int e, row0, nrows, fb;
             item_rows<GATEUP>(p, item, e, row0, nrows, fb);
-            const int buf = ic & 1;
-            const uint32_t aph = (ic >> 1) & 1;
-            bool ok = tc::mbar_wait(bar_accfull + 8 * buf, aph, abort_flag, p.err);
+            const uint32_t aph = ic & 1;
+            bool ok = tc::mbar_wait(bar_accfull, aph, abort_flag, p.err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::tc_fence_after();
             const int ncb = ceil_div(nrows, 32);
-            for (int cb = 0; cb < ncb; ++cb) {
+            const int last = ncb - 1 - ((ncb - 1 - eh) & 1);  // this warp's last block (< eh: none)
+            for (int cb = eh; cb < ncb; cb += 2) {
                 uint32_t v[32];
-                tc::tmem_ld_32x32b_x32(tmem_base + buf * 256 + cb * 32 + ((uint32_t)(32 * q) << 16), v);
+                tc::tmem_ld_32x32b_x32(tmem_base + cb * 32 + ((uint32_t)(32 * q) << 16), v);
                 tc::tmem_ld_wait();
+                if (cb == last) {
+                    // every column read: the MMA warp may start the next item
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(bar_accempty);
+                }
                 // out-of-range fp16 values are collected per column block and
                 // reported once (a branch per element costs more than the math)
                 uint32_t bad = 0;
@@ -395,9 +403,11 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 }
                 if (bad) set_error(p.err, ERRBIT_F16_RANGE);
             }
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar_accempty + 8 * buf);
+            if (last < eh) {
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar_accempty);
+            }
         }
     }
 
@@ -437,6 +447,18 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* 
     cuuint32_t estr[2] = {1, 1};
     return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t TC_SMEM_LIMIT = 232448;
+
+// Stages for a reduction length: as many as fit (4 .. 6).  A stage must be
+// refilled while the MMAs of the stages ahead of it run: the copy latency
+// (about a microsecond) plus the dequantisation has to fit in S - 1 stages'
+// MMA time, so deeper rings keep the tensor pipe fed.
+int tc_stages(int K) {
+    for (int st = 6; st > 4; --st)
+        if (tc_smem_bytes(st, K) <= TC_SMEM_LIMIT) return st;
+    return 4;
 }
 
 template <bool GATEUP, int S>
@@ -483,7 +505,7 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<GATEUP, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)tc_smem_bytes(S, S == 4 ? 2048 : 8192));
+                                             (int)TC_SMEM_LIMIT);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -493,8 +515,6 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
     note_launch();
     return cudaGetLastError();
 }
-
-constexpr size_t TC_SMEM_LIMIT = 232448;
 
 }  // namespace
 
@@ -544,21 +564,26 @@ int tc_max_tiles(int R, int E) { return ceil_div(R, TILE_ROWS) + std::min(R, E);
 bool tc_supported(int E, int d, int f) {
     (void)E;
     if (d % 256 || f % 256) return false;
-    // 4 stages while the scale buffers fit, else 3
     const int Kmax = std::max(d, f);
-    return tc_smem_bytes(3, Kmax) <= TC_SMEM_LIMIT && d <= 8192 && f <= 8192;
+    return tc_smem_bytes(4, Kmax) <= TC_SMEM_LIMIT && d <= 8192 && f <= 8192;
 }
 
 cudaError_t launch_tc_gateup(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
-    if (tc_smem_bytes(4, d) <= TC_SMEM_LIMIT) return launch_impl<true, 4>(E, d, f, R, in, s);
-    return launch_impl<true, 3>(E, d, f, R, in, s);
+    switch (tc_stages(d)) {
+        case 6: return launch_impl<true, 6>(E, d, f, R, in, s);
+        case 5: return launch_impl<true, 5>(E, d, f, R, in, s);
+        default: return launch_impl<true, 4>(E, d, f, R, in, s);
+    }
 }
 
 cudaError_t launch_tc_down(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
-    if (tc_smem_bytes(4, f) <= TC_SMEM_LIMIT) return launch_impl<false, 4>(E, d, f, R, in, s);
-    return launch_impl<false, 3>(E, d, f, R, in, s);
+    switch (tc_stages(f)) {
+        case 6: return launch_impl<false, 6>(E, d, f, R, in, s);
+        case 5: return launch_impl<false, 5>(E, d, f, R, in, s);
+        default: return launch_impl<false, 4>(E, d, f, R, in, s);
+    }
 }
 
 }  // namespace moe
