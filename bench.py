@@ -190,9 +190,8 @@ class Workload:
 
 
 def decode_kernel_name():
-    """The one-kernel decode layer the library runs (MOE_W4_DECODE_KERNEL=flow
-    picks the dataflow kernel instead of the default grid-barrier kernel)."""
-    return "decode_flow_kernel" if os.environ.get("MOE_W4_DECODE_KERNEL") == "flow" else "decode_fused_kernel"
+    """The one-kernel decode layer the library runs."""
+    return "decode_fused_kernel"
 
 
 def expert_bytes(cfg, which):

@@ -123,8 +123,7 @@ struct LayerWs {
     int32_t *ids, *counts, *offsets, *sorted, *inv;
     float* w;
     float* h;             // fp32 [R][f] (GEMV regime) or fp16 [R][f] (tensor-core regime)
-    uint16_t *x_perm, *y_perm;  // fp16 [R][d] (tensor-core regime); together the
-                                // dataflow decode kernel's fp32 [R][d] y rows
+    uint16_t *x_perm, *y_perm;  // fp16 [R][d] (tensor-core regime)
     size_t bytes;
 };
 
@@ -132,9 +131,6 @@ LayerWs carve_layer(void* ws, int T, int k, int E, int d, int f) {
     const int R = T * k;
     Carver c(ws);
     LayerWs l;
-    // the dataflow decode kernel's counters sit right after the header, where
-    // moe_get_device_error can clear them
-    c.take<unsigned char>(flow_counter_bytes(T, d));
     l.ps = carve_perm(c, R, E);
     l.ids = c.take<int32_t>(R);
     l.w = c.take<float>(R);
@@ -167,16 +163,13 @@ FfnWs carve_ffn(void* ws, int R, int E, int d, int f) {
 }
 
 // The decode regime of moe_layer_forward runs as one kernel when the shape
-// allows: the grid-barrier kernel, else the route/permute/GEMV chain.
-// MOE_W4_DECODE_KERNEL=fused|flow|split picks one (flow: the dataflow kernel;
-// a kernel that does not support the shape falls back to the chain).
-enum class DecodeKernel { Flow, Fused, Split };
+// allows (the grid-barrier kernel), else as the route/permute/GEMV chain;
+// MOE_W4_DECODE_KERNEL=split forces the chain.
+enum class DecodeKernel { Fused, Split };
 
 DecodeKernel pick_decode_kernel(int T, int k, const moe_w4_layer* L) {
     const char* v = std::getenv("MOE_W4_DECODE_KERNEL");
     if (v && !std::strcmp(v, "split")) return DecodeKernel::Split;
-    if (v && !std::strcmp(v, "flow"))
-        return decode_flow_supported(T, k, L->E, L->d_model, L->d_ff) ? DecodeKernel::Flow : DecodeKernel::Split;
     if (decode_fused_supported(T, k, L->E, L->d_model, L->d_ff)) return DecodeKernel::Fused;
     return DecodeKernel::Split;
 }
@@ -385,9 +378,8 @@ moe_status_t moe_layer_forward(const moe_w4_layer* L, const void* x_bf16, const 
                    static_cast<uint16_t*>(out_bf16),
                    topk_ids_out,
                    reinterpret_cast<uint16_t*>(w.h),
-                   reinterpret_cast<float*>(w.x_perm),
                    workspace};
-        const cudaError_t fe = dk == DecodeKernel::Flow ? launch_decode_flow(fi, stream) : launch_decode_fused(fi, stream);
+        const cudaError_t fe = launch_decode_fused(fi, stream);
         for (int i = 1; i <= 5; ++i) marks.mark(i);
         return cuda_status(fe);
     }
@@ -453,13 +445,12 @@ uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_re
 moe_status_t moe_get_device_error(void* workspace, cudaStream_t stream) {
     if (!workspace) return MOE_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
-    uint32_t hw[2] = {0, 0};  // error word, bytes of counters kept between CTAs
-    if (cudaMemcpy(hw, workspace, sizeof(hw), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-    const uint32_t e = hw[0];
+    uint32_t e = 0;
+    if (cudaMemcpy(&e, workspace, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
     if (e == 0) return MOE_OK;
-    // the header and the counters a call that gave up may have left behind
-    const size_t clear = std::max<size_t>(WS_HEADER, std::min<size_t>(hw[1], (size_t)1 << 20));
-    if (cudaMemset(workspace, 0, clear) != cudaSuccess) return MOE_ERR_CUDA;
+    // the header: the error word and whatever a call that gave up left behind
+    // (the grid-barrier kernel's arrival counter)
+    if (cudaMemset(workspace, 0, WS_HEADER) != cudaSuccess) return MOE_ERR_CUDA;
     if (e & ERRBIT_TIMEOUT) return MOE_ERR_TIMEOUT;
     if (e & ERRBIT_RANGE) return MOE_ERR_DEVICE_RANGE;
     return MOE_ERR_F16_RANGE;

@@ -26,19 +26,8 @@ struct WsHeader {
     uint32_t err;        // OR of ERRBIT_*; cleared by moe_get_device_error
     uint32_t reserved[63];
 };
-// Header words of the one-kernel decode layers (32-bit word indexes):
-//   WS_CLEAR_WORD  bytes from the start of the workspace that hold counters a
-//                  call keeps between its CTAs (header included); written by
-//                  every such call, read by moe_get_device_error, which clears
-//                  that many bytes after an error (a call that gave up can
-//                  leave counters behind)
-//   WS_ABORT_WORD  set when any CTA of the dataflow kernel gave up a wait
-//   WS_BAR_COUNT_WORD  the grid-barrier kernel's 64-bit arrival counter (its
-//                  own 64-byte sector)
-// The dataflow kernel's per-expert and per-(token, row block) counters follow
-// the header, at byte WS_HEADER.
-constexpr int WS_CLEAR_WORD = 1;
-constexpr int WS_ABORT_WORD = 3;
+// Header word of the one-kernel decode layer (32-bit word index): the
+// grid-barrier kernel's 64-bit arrival counter, in its own 64-byte sector.
 constexpr int WS_BAR_COUNT_WORD = 16;
 
 // Small device-side plan written by the permutation kernels (after the header).

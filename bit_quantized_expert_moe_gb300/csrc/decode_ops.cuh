@@ -1,7 +1,7 @@
-// Device helpers shared by the one-kernel decode layers: the int4 chunk
-// format of the shared-memory ring, routing in registers, the staged fp16
-// activation layout and the m16n8k16 group product on register-dequantised
-// codes.  See decode_flow.cu for how they are put together.
+// Device helpers of the decode regime: the int4 chunk format of the
+// shared-memory ring, routing in registers (also used by the router kernel),
+// the staged fp16 activation layout and the m16n8k16 group product on
+// register-dequantised codes.  decode_fused.cu puts them together.
 #pragma once
 
 #include <cfloat>

@@ -99,17 +99,10 @@ struct FusedIn {
     uint16_t* out;           // bf16 [T][d]
     int32_t* ids_out;        // [T][k] or null
     uint16_t* hb;            // fp16 scratch, [T*k][f]
-    float* ybuf;             // fp32 scratch, [T*k][d] (dataflow kernel)
     void* ws;                // workspace (header: error word and the kernels' counters)
 };
 bool decode_fused_supported(int T, int k, int E, int d, int f);
 cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s);
-// The same layer as a dataflow kernel without a grid barrier (decode_flow.cu).
-// Its counters take flow_counter_bytes(T, d) bytes right after the workspace
-// header.
-bool decode_flow_supported(int T, int k, int E, int d, int f);
-cudaError_t launch_decode_flow(const FusedIn& in, cudaStream_t s);
-size_t flow_counter_bytes(int T, int d);
 
 // ---------------------------------------------- prefill regime (tcgen05)
 struct TcIn {

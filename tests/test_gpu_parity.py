@@ -299,7 +299,7 @@ def test_zero_tokens_is_a_no_op(M):
 
 
 # ------------------------------------------- decode regime: one-kernel layer
-@pytest.mark.parametrize("kernel", ["flow", "fused", "split"])
+@pytest.mark.parametrize("kernel", ["fused", "split"])
 @pytest.mark.parametrize("name", ["tiny", "decode", "large_decode"])
 def test_decode_layer_kernels_match_oracle(M, decode_kernel, kernel, name):
     cfg = S.CONFIGS[name]
@@ -449,70 +449,3 @@ def test_fused_decode_back_to_back_calls_on_one_workspace(M, name):
     assert M.get_device_error(ws) == 0
     for o, l in zip(outs, seq):
         assert torch.equal(o.view(torch.int16), ref[l].view(torch.int16))
-
-
-# ------------------------------------------- decode regime: dataflow kernel
-# Byte offsets in a layer workspace: the header's words 1 (bytes of counters
-# kept between CTAs) and 3 (abort flag), then, from byte 256, the readiness
-# counter of each touched expert.
-_CLEAR_WORD, _ABORT_WORD, _COUNTERS = 1, 3, 256
-
-
-def test_flow_decode_calls_return_their_counters_to_zero(M):
-    """The dataflow kernel keeps counters in the workspace (per expert
-    readiness and down units, per (token, row block) contributions); every call must
-    leave them at zero, so that calls on one workspace keep working and agree
-    with the oracle."""
-    import torch
-    cfg = S.CONFIGS["decode"]
-    layers = [M.Layer.from_numpy(_layer(cfg, l)) for l in (0, 1)]
-    ws = M.workspace(max(M.layer_workspace_size(ly, cfg.T, cfg.k) for ly in layers))
-    calls = [M.LayerCall(ly, cfg.T, cfg.k, ws=ws) for ly in layers]
-    outs = []
-    for l in (0, 1, 0, 1, 0):
-        o = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
-        calls[l](x_to_dev(S.activations(cfg, l)), f32_to_dev(S.router_logits(cfg, l)), o)
-        outs.append(o)
-    torch.cuda.synchronize()
-    hdr = ws[:256].view(torch.int32).cpu().numpy()
-    clear = int(hdr[_CLEAR_WORD])
-    assert clear > _COUNTERS, "the kernel must record the size of its counters"
-    assert hdr[0] == 0 and hdr[_ABORT_WORD] == 0
-    assert int(ws[_COUNTERS:clear].count_nonzero()) == 0
-    for a, b in ((0, 2), (0, 4), (1, 3)):
-        assert torch.equal(outs[a].view(torch.int16), outs[b].view(torch.int16))
-    for l in (0, 1):
-        ref = OM.layer_forward(S.activations(cfg, l), S.router_logits(cfg, l), _getter(_layer(cfg, l)), cfg.E,
-                               cfg.d, cfg.f, cfg.k)
-        assert_close(bf16_to_f64(outs[l]), ref, f"flow repeated, layer {l}")
-
-
-def test_flow_decode_wait_that_runs_out_reports_a_timeout(M):
-    """A bounded wait that runs out: the first touched expert's readiness
-    counter is set to a value its gate_up units can never bring to the target,
-    so every down unit of that expert waits until the 2 s limit.  The call
-    must end (no hang), report MOE_ERR_TIMEOUT, and after moe_get_device_error
-    has cleared the workspace's counters the next call on the same workspace
-    must match the oracle again."""
-    import torch
-    cfg = S.CONFIGS["decode"]
-    W = _layer(cfg, 0)
-    layer = M.Layer.from_numpy(W)
-    call = M.LayerCall(layer, cfg.T, cfg.k)
-    x, lg = x_to_dev(S.activations(cfg, 0)), f32_to_dev(S.router_logits(cfg, 0))
-    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
-    call(x, lg, out)
-    assert M.get_device_error(call.ws) == 0
-    clear = int(call.ws[:256].view(torch.int32).cpu().numpy()[_CLEAR_WORD])
-    assert clear > _COUNTERS
-    call.ws[_COUNTERS:_COUNTERS + 4].view(torch.int32).fill_(1 << 30)
-    call(x, lg, out)
-    assert M.get_device_error(call.ws) == 7  # MOE_ERR_TIMEOUT
-    hdr = call.ws[:256].view(torch.int32).cpu().numpy()
-    assert hdr[0] == 0 and hdr[_ABORT_WORD] == 0
-    assert int(call.ws[_COUNTERS:clear].count_nonzero()) == 0
-    out.zero_()
-    call(x, lg, out)
-    assert M.get_device_error(call.ws) == 0
-    ref = OM.layer_forward(S.activations(cfg, 0), S.router_logits(cfg, 0), _getter(W), cfg.E, cfg.d, cfg.f, cfg.k)
-    assert_close(bf16_to_f64(out), ref, "flow after a timeout")
