@@ -143,11 +143,12 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     uint16_t* sScale = reinterpret_cast<uint16_t*>(gbase + S * STAGE_BYTES);  // [2][BM][G]
     uint16_t* sZero = sScale + 2 * BM * G;                                     // [2][BM][G]
     const uint32_t bars = base + S * STAGE_BYTES + (uint32_t)scale_bytes(p.K);
-    // barrier layout: full[S], afull[S], empty[S], accfull[2], accempty[2], done
+    // barrier layout: full[S], afull[S], empty[S], accfull[2], accempty[2], done, qsync[4]
     // (one accumulator: only accfull[0] and accempty[0] are used)
     const uint32_t bar_full = bars, bar_afull = bars + 8 * S, bar_empty = bars + 16 * S;
     const uint32_t bar_accfull = bars + 24 * S, bar_accempty = bar_accfull + 16, bar_done = bar_accempty + 16;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + S * STAGE_BYTES + scale_bytes(p.K) + 8 * (3 * S + 5));
+    const uint32_t bar_qsync = bar_done + 8;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + S * STAGE_BYTES + scale_bytes(p.K) + 8 * (3 * S + 9));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -165,6 +166,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             tc::mbar_init(bar_accempty + 8 * b, EP_WARPS);
         }
         tc::mbar_init(bar_done, 1);
+        for (int q4 = 0; q4 < 4; ++q4) tc::mbar_init(bar_qsync + 8 * q4, 2);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -257,14 +259,29 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         // ------------------------------------------------------ dequantisers
         // Warp w owns A row r = 32 (w % 4) + lane (its TMEM lane) and half
         // hk = (w - 4) / 4 of every stage's K: 4 packed words (32 codes) per
-        // stage, widened in registers and stored as 16 TMEM columns.  Each
-        // warp prefetches the scales and zeros of the rows it reads (4-byte
-        // cp.async; the two warps of a lane quarter copy the same values), so
-        // only warp-level synchronisation is needed.  Waits are warp-uniform.
+        // stage, widened in registers and stored as 16 TMEM columns.  The two
+        // warps of a lane quarter share its rows' scales and zeros: warp hk
+        // prefetches array hk (scales, zeros) of the next item into the other
+        // half of a double buffer (4-byte cp.async).  They meet on a named
+        // mbarrier at every item start, after which both are done with the
+        // previous item's buffer (the one the next prefetch overwrites), and
+        // again once both copies of this item have landed.  Every wait is
+        // bounded and warp-uniform, so a warp whose partner gave up leaves too.
         const int q = warp & 3, hk = (warp - DQ_WARP0) >> 2;
         const int r = 32 * q + lane;
         const int prow = a_packed_row<GATEUP>(r);
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
+        const uint32_t qbar = bar_qsync + 8 * q;  // the quarter's two warps meet here
+        uint32_t qphase = 0;
+        auto quarter_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(qbar);
+            const bool r = tc::mbar_wait(qbar, qphase, abort_flag, p.err);
+            qphase ^= 1u;
+            return __all_sync(0xffffffffu, r);
+        };
+        uint16_t* const s_dst = hk ? sZero : sScale;
+        const uint16_t* const s_src = hk ? p.wz : p.wsc;
         auto prefetch_scales = [&](int item, int buf) {
             int e, row0, nrows, fb;
             item_rows<GATEUP>(p, item, e, row0, nrows, fb);
@@ -272,10 +289,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             for (int idx = lane; idx < 32 * pairs; idx += 32) {
                 const int rr = 32 * q + idx / pairs, gp = idx % pairs;
                 const size_t grow = a_global_row<GATEUP>(p, e, fb, rr);
-                const size_t src = grow * G + 2 * gp;
-                const size_t dst = ((size_t)buf * BM + rr) * G + 2 * gp;
-                cp_async4(smem_u32(sScale + dst), p.wsc + src);
-                cp_async4(smem_u32(sZero + dst), p.wz + src);
+                cp_async4(smem_u32(s_dst + ((size_t)buf * BM + rr) * G + 2 * gp), s_src + grow * G + 2 * gp);
             }
         };
         int stage = 0;
@@ -286,11 +300,13 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         cp_async_commit();
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
             const int sbuf = ic & 1;
-            __syncwarp();  // the warp is done with the buffer the next prefetch overwrites
+            // both warps are done with the buffer the next prefetch overwrites
+            if (!quarter_sync()) break;
             if (item + (int)gridDim.x < n_items) prefetch_scales(item + gridDim.x, sbuf ^ 1);
             cp_async_commit();
             cp_async_wait<1>();
-            __syncwarp();  // this item's scales visible to the whole warp
+            // both warps' copies of this item's scales and zeros have landed
+            if (!quarter_sync()) break;
             uint32_t s2 = 0, nzs2 = 0;  // as f16x2: (s, s) and (-fl16(z s), -fl16(z s))
             for (int kc = 0; kc < NK; ++kc) {
                 ok = tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err);
