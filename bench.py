@@ -327,14 +327,36 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
         peak = float(peaks["bf16_tflops"])
         both = (fl_gu + fl_dn) / (t_gu + t_dn) / 1e12
         tr = traffic_for("tc_gateup_" + wl.name)
-        roofline = {"bound": "tensor", "kernel": "tc_grouped_kernel<gate_up>", "achieved": round(achieved, 1),
-                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                    "traffic": (round(tr["dram_bytes_per_launch"]) if tr else None),
-                    "flops_per_launch": fl_gu, "avg_launch_us": round(t_gu * 1e6, 2), "peak_source": peak_src,
-                    "expert_gemms_pair": {"achieved": round(both, 1), "frac": round(both / peak, 4),
-                                          "down_avg_us": round(t_dn * 1e6, 2)},
-                    "weight_bytes_touched": float(sum(uniq) / len(uniq) * (expert_bytes(cfg, "gate_up") +
-                                                                          expert_bytes(cfg, "down")))}
+        wb_gu = float(sum(uniq) / len(uniq) * expert_bytes(cfg, "gate_up"))
+        wb_dn = float(sum(uniq) / len(uniq) * expert_bytes(cfg, "down"))
+        # The bound follows the arithmetic intensity: FLOPs per byte of the
+        # expert weights the GEMM must read, against the ridge point of the
+        # measured peaks.  Few tokens per expert (P=512 over 128 or 256
+        # experts) put the grouped GEMM on the HBM side of the ridge.
+        hbm_peak = float(peaks["hbm_gbs"])
+        intensity = fl_gu / wb_gu
+        ridge = peak * 1e12 / (hbm_peak * 1e9)
+        if intensity >= ridge:
+            roofline = {"bound": "tensor", "kernel": "tc_grouped_kernel<gate_up>", "achieved": round(achieved, 1),
+                        "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                        "traffic": (round(tr["dram_bytes_per_launch"]) if tr else None),
+                        "flops_per_launch": fl_gu, "avg_launch_us": round(t_gu * 1e6, 2), "peak_source": peak_src,
+                        "expert_gemms_pair": {"achieved": round(both, 1), "frac": round(both / peak, 4),
+                                              "down_avg_us": round(t_dn * 1e6, 2)}}
+        else:
+            gbs = wb_gu / t_gu / 1e9
+            gbs_pair = (wb_gu + wb_dn) / (t_gu + t_dn) / 1e9
+            roofline = {"bound": "hbm", "kernel": "tc_grouped_kernel<gate_up>", "achieved": round(gbs, 1),
+                        "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                        "traffic": (round(tr["dram_bytes_per_launch"]) if tr else None),
+                        "algorithmic_bytes_per_launch": wb_gu, "avg_launch_us": round(t_gu * 1e6, 2),
+                        "peak_source": peak_src,
+                        "tensor": {"achieved_tflops": round(achieved, 1), "frac_of_bf16_peak": round(achieved / peak, 4)},
+                        "expert_gemms_pair": {"achieved": round(gbs_pair, 1), "frac": round(gbs_pair / hbm_peak, 4),
+                                              "down_avg_us": round(t_dn * 1e6, 2)}}
+        roofline["arithmetic_intensity_flop_per_weight_byte"] = round(intensity, 1)
+        roofline["ridge_flop_per_byte"] = round(ridge, 1)
+        roofline["weight_bytes_touched"] = wb_gu + wb_dn
     if fused:
         # one launch holds every stage: only the bracket around it means
         # anything (its event-record nodes also stop consecutive launches from
