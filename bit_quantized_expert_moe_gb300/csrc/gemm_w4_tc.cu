@@ -32,11 +32,11 @@
 // down: 128 consecutive rows of W2; the epilogue writes y rows (fp16 for the
 // layer's own combine, bf16 when y is the caller's output).
 //
-// Warp roles (768 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
+// Warp roles (896 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
 // 2-3 idle, 4-11 dequantisation (warp w: TMEM lane quarter w % 4, half
-// (w - 4) / 4 of a stage's K), 12-23 epilogue (warp w: lane quarter w % 4,
-// every third 32-column block).  With one accumulator the next item's MMAs
-// wait until the epilogue has read it, so three warps per quarter cut that
+// (w - 4) / 4 of a stage's K), 12-27 epilogue (warp w: lane quarter w % 4,
+// every fourth 32-column block).  With one accumulator the next item's MMAs
+// wait until the epilogue has read it, so four warps per quarter cut that
 // wait.
 // TMEM: the fp32 accumulator in columns 0..255, stage s's A in columns
 // 256 + 32 s .. + 31.
@@ -58,9 +58,9 @@ constexpr int P_BYTES = BM * BK / 2;     // 4 KB of packed codes
 constexpr int STAGE_BYTES = B_BYTES + P_BYTES;
 constexpr int B_BOX_ROWS = 64;           // activation rows per TMA box (fewer, larger copies: the single producer thread issues every one)
 constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
-constexpr int THREADS = 768;
+constexpr int THREADS = 896;
 constexpr int DQ_WARP0 = 4, DQ_WARPS = 8;
-constexpr int EP_WARP0 = 12, EP_WARPS = 12;
+constexpr int EP_WARP0 = 12, EP_WARPS = 16;
 constexpr uint32_t TMEM_COLS = 512;      // accumulator (256 columns) + S <= 6 A stages of 32 columns
 constexpr uint32_t A_COL0 = 256;         // first TMEM column of stage 0's A
 constexpr uint32_t A_STAGE_COLS = BK / 2;
@@ -348,7 +348,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     } else if (warp >= EP_WARP0) {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM lane quarter
-        const int eh = (warp - EP_WARP0) >> 2;  // column blocks eh, eh + 3, ...
+        const int eh = (warp - EP_WARP0) >> 2;  // column blocks eh, eh + EP_WARPS / 4, ...
         int ic = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ic) {
             int e, row0, nrows, fb;
@@ -359,8 +359,9 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             tc::tc_fence_after();
             const int ncb = ceil_div(nrows, 32);
             // this warp's last block (< eh: none)
-            const int last = ncb - 1 < eh ? -1 : eh + 3 * ((ncb - 1 - eh) / 3);
-            for (int cb = eh; cb < ncb; cb += 3) {
+            constexpr int EP_STEP = EP_WARPS / 4;
+            const int last = ncb - 1 < eh ? -1 : eh + EP_STEP * ((ncb - 1 - eh) / EP_STEP);
+            for (int cb = eh; cb < ncb; cb += EP_STEP) {
                 uint32_t v[32];
                 tc::tmem_ld_32x32b_x32(tmem_base + cb * 32 + ((uint32_t)(32 * q) << 16), v);
                 tc::tmem_ld_wait();
