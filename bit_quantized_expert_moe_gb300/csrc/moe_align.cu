@@ -7,11 +7,15 @@
 // bit-exactly.
 //
 // Small batches (R <= ALIGN_SMALL_MAX_R) use one CTA for everything.  Larger
-// batches use: per-block histograms -> one scan CTA -> per-block stable
-// scatter (one warp walks its block's assignments in order) -> row gather.
-// Besides counts/offsets/sorted/inv the scan also emits the list of experts
-// with rows (for the GEMV regime) and the token tiles (for the tensor-core
-// regime).  An id outside [0, E) sets the range error bit and is skipped.
+// batches use two kernels: per-block histograms, then one CTA per block that
+// sums the earlier blocks' counts and every block's counts straight from the
+// count table, scans the totals into expert offsets, places its block's
+// assignments in order (one warp, stable) and copies their activation rows
+// (all warps; a separate row gather when there are too few blocks to fill
+// the GPU).  Besides counts/offsets/sorted/inv, block 0 also emits the list
+// of experts with rows (for the GEMV regime) and the token tiles (for the
+// tensor-core regime).  An id outside [0, E) sets the range error bit and is
+// skipped.
 #include "internal.h"
 
 namespace moe {
@@ -92,10 +96,11 @@ __device__ void emit_plan(int cnt, int e, int E, int32_t* counts, int32_t* offse
 
 // Stable placement of assignments [a0, a1) by one warp, walking them in
 // ascending order 32 at a time.  The id of assignment a is ids[a - ibase];
-// run[e] holds the next free position of e.
+// run[e] holds the next free position of e.  When pos_out is given,
+// pos_out[a - ibase] receives a's position (-1 for an id outside [0, E)).
 __device__ void warp_stable_scatter(const int32_t* __restrict__ ids, int ibase, int a0, int a1, int E, int* run,
                                     int32_t* __restrict__ sorted, int32_t* __restrict__ inv,
-                                    uint32_t* err) {
+                                    uint32_t* err, int32_t* pos_out = nullptr) {
     const int lane = threadIdx.x & 31;
     const uint32_t lt = (1u << lane) - 1u;
     for (int base = a0; base < a1; base += 32) {
@@ -110,6 +115,9 @@ __device__ void warp_stable_scatter(const int32_t* __restrict__ ids, int ibase, 
             const int pos = run[e] + rank;
             sorted[pos] = a;
             inv[a] = pos;
+            if (pos_out) pos_out[a - ibase] = pos;
+        } else if (pos_out && a < a1) {
+            pos_out[a - ibase] = -1;
         }
         __syncwarp();
         if (valid && (__ffs(peers) - 1) == lane) run[e] += __popc(peers);
@@ -124,38 +132,45 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, bool& bad) {
     return r;
 }
 
-// Copy rows x[sorted[i] / k] -> x_perm[i] for i in [i0, i1), 16 bytes per lane,
+// One activation row (d elements) copied by a warp, 16 bytes per lane,
 // converting bf16 to fp16 when TO_F16 (then in the tensor-core operand order:
-// K interleaved in groups of 8, see k8_interleave).
+// K interleaved in groups of 8, see k8_interleave).  8 vectors per lane at a
+// time, all loads in flight before the stores.
+template <bool TO_F16>
+__device__ __forceinline__ void copy_row(const uint16_t* __restrict__ src_row, uint16_t* __restrict__ dst_row, int d,
+                                         int lane, bool& bad) {
+    const int vec = d / 8;  // 16-byte vectors per row
+    const uint4* src = reinterpret_cast<const uint4*>(src_row);
+    uint4* dst = reinterpret_cast<uint4*>(dst_row);
+    for (int v0 = 0; v0 < vec; v0 += 256) {
+        uint4 q[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int v = v0 + lane + 32 * u;
+            if (v < vec) q[u] = src[v];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int v = v0 + lane + 32 * u;
+            if (v >= vec) break;
+            if (TO_F16)
+                q[u] = k8_interleave(bf16x2_to_f16x2(q[u].x, bad), bf16x2_to_f16x2(q[u].y, bad),
+                                     bf16x2_to_f16x2(q[u].z, bad), bf16x2_to_f16x2(q[u].w, bad));
+            dst[v] = q[u];
+        }
+    }
+}
+
+// Copy rows x[sorted[i] / k] -> x_perm[i] for i in [i0, i1), one warp a row.
 template <bool TO_F16>
 __device__ void gather_rows(const uint16_t* __restrict__ x, int d, int k, const int32_t* __restrict__ sorted,
                             int i0, int i1, uint16_t* __restrict__ x_perm, int warp, int nwarps, uint32_t* err) {
     const int lane = threadIdx.x & 31;
-    const int vec = d / 8;  // 16-byte vectors per row
     bool bad = false;
     for (int i = i0 + warp; i < i1; i += nwarps) {
         const int a = sorted[i];
         if (a < 0 || a >= i1) continue;  // a slot left unwritten by out-of-range ids
-        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(a / k) * d);
-        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)i * d);
-        // 8 vectors per lane at a time, all loads in flight before the stores
-        for (int v0 = 0; v0 < vec; v0 += 256) {
-            uint4 q[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int v = v0 + lane + 32 * u;
-                if (v < vec) q[u] = src[v];
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int v = v0 + lane + 32 * u;
-                if (v >= vec) break;
-                if (TO_F16)
-                    q[u] = k8_interleave(bf16x2_to_f16x2(q[u].x, bad), bf16x2_to_f16x2(q[u].y, bad),
-                                         bf16x2_to_f16x2(q[u].z, bad), bf16x2_to_f16x2(q[u].w, bad));
-                dst[v] = q[u];
-            }
-        }
+        copy_row<TO_F16>(x + (size_t)(a / k) * d, x_perm + (size_t)i * d, d, lane, bad);
     }
     if (TO_F16 && bad) set_error(err, ERRBIT_F16_RANGE);
 }
@@ -210,44 +225,78 @@ __global__ void __launch_bounds__(256) align_hist_kernel(const int32_t* __restri
     for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[(size_t)blockIdx.x * E + e] = cnt[e];
 }
 
-// Turns blockcnt[b][e] into the first position of block b's assignments to e.
-// Thread e walks the blocks in batches whose loads are all issued before any
-// store, so the batch costs one memory latency rather than one per block.
-__global__ void __launch_bounds__(SCAN_THREADS) align_scan_kernel(int nblocks, int E, int32_t* __restrict__ blockcnt,
-                                                                  AlignOut o) {
-    constexpr int BATCH = 16;
-    const int e = threadIdx.x;
-    int total = 0;
-    if (e < E) {
-        for (int b0 = 0; b0 < nblocks; b0 += BATCH) {
-            int c[BATCH];
-#pragma unroll
-            for (int i = 0; i < BATCH; ++i) c[i] = b0 + i < nblocks ? blockcnt[(size_t)(b0 + i) * E + e] : 0;
-#pragma unroll
-            for (int i = 0; i < BATCH; ++i) {
-                if (b0 + i < nblocks) blockcnt[(size_t)(b0 + i) * E + e] = total;
-                total += c[i];
-            }
-        }
-    }
-    int off = 0;
-    emit_plan(total, e, E, o.counts, o.offsets, o.uniq, o.tiles, o.plan, &off);
-    if (e < E)
-        for (int b = 0; b < nblocks; ++b) blockcnt[(size_t)b * E + e] += off;
-}
-
-// One warp per block of assignments: the block's ids are first copied to
-// shared memory with all loads in flight at once, then placed in order.
-__global__ void __launch_bounds__(32) align_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int rows,
-                                                           const int32_t* __restrict__ blockcnt, AlignOut o) {
+// One CTA (SCAN_THREADS threads) per block of assignments b:
+//  1. per expert e, the assignments to e in blocks before b and in all blocks,
+//     read from the count table by SCAN_THREADS / E thread groups, each
+//     summing a contiguous slice of the blocks with all its loads in flight;
+//  2. the expert offsets (exclusive scan of the totals; block 0 also writes
+//     counts, offsets, the experts with rows and the token tiles);
+//  3. the stable placement of block b's assignments by warp 0 from
+//     run[e] = offset[e] + (assignments to e in earlier blocks);
+//  4. with COPY, every warp copies activation rows of the block's
+//     assignments to their positions in x_perm.
+template <bool COPY>
+__global__ void __launch_bounds__(SCAN_THREADS) align_place_kernel(const int32_t* __restrict__ ids, int R, int k, int E,
+                                                                   int rows, int nblocks,
+                                                                   const int32_t* __restrict__ blockcnt,
+                                                                   const uint16_t* __restrict__ x, int d, AlignOut o) {
+    __shared__ int s_pre[SCAN_THREADS];
+    __shared__ int s_tot[SCAN_THREADS];
     __shared__ int run[1024];
     __shared__ int32_t bid[ALIGN_BLOCK_ROWS];
-    const int a0 = blockIdx.x * rows;
-    const int a1 = min(R, a0 + rows);
-    for (int e = threadIdx.x; e < E; e += 32) run[e] = blockcnt[(size_t)blockIdx.x * E + e];
-    for (int a = a0 + threadIdx.x; a < a1; a += 32) bid[a - a0] = ids[a];
-    __syncwarp();
-    warp_stable_scatter(bid, a0, a0, a1, E, run, o.sorted, o.inv, o.err);
+    __shared__ int32_t pos[ALIGN_BLOCK_ROWS];
+    const int tid = threadIdx.x, b = blockIdx.x;
+    const int a0 = b * rows, a1 = min(R, a0 + rows);
+    for (int a = a0 + tid; a < a1; a += SCAN_THREADS) bid[a - a0] = ids[a];
+    const int groups = SCAN_THREADS / E;  // >= 1 since E <= 1024
+    if (tid < groups * E) {
+        const int e = tid % E, j = tid / E;
+        const int b_lo = (int)((long long)j * nblocks / groups);
+        const int b_hi = (int)((long long)(j + 1) * nblocks / groups);
+        constexpr int BATCH = 16;
+        int pre = 0, tot = 0;
+        for (int c0 = b_lo; c0 < b_hi; c0 += BATCH) {
+            int c[BATCH];
+#pragma unroll
+            for (int i = 0; i < BATCH; ++i) c[i] = c0 + i < b_hi ? blockcnt[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+            for (int i = 0; i < BATCH; ++i) {
+                tot += c[i];
+                if (c0 + i < b) pre += c[i];
+            }
+        }
+        s_pre[tid] = pre;
+        s_tot[tid] = tot;
+    }
+    __syncthreads();
+    int pre = 0, tot = 0;
+    if (tid < E)
+        for (int j = 0; j < groups; ++j) {
+            pre += s_pre[j * E + tid];
+            tot += s_tot[j * E + tid];
+        }
+    const bool lead = b == 0;
+    int off = 0;
+    emit_plan(tot, tid, E, lead ? o.counts : nullptr, lead ? o.offsets : nullptr, lead ? o.uniq : nullptr,
+              lead ? o.tiles : nullptr, lead ? o.plan : nullptr, &off);
+    if (tid < E) run[tid] = off + pre;
+    __syncthreads();
+    if (tid < 32) warp_stable_scatter(bid, a0, a0, a1, E, run, o.sorted, o.inv, o.err, pos);
+    if (COPY) {
+        __syncthreads();
+        const int lane = tid & 31;
+        bool bad = false;
+        for (int i = tid >> 5; i < a1 - a0; i += SCAN_THREADS / 32) {
+            const int p = pos[i];
+            if (p < 0) continue;
+            const uint16_t* src = x + (size_t)((a0 + i) / k) * d;
+            if (o.x_perm_f16)
+                copy_row<true>(src, o.x_perm + (size_t)p * d, d, lane, bad);
+            else
+                copy_row<false>(src, o.x_perm + (size_t)p * d, d, lane, bad);
+        }
+        if (bad) set_error(o.err, ERRBIT_F16_RANGE);
+    }
 }
 
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int d, int k, int R, AlignOut o) {
@@ -296,11 +345,15 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, const uint16_t
     const int nb = ceil_div(R, rows);
     align_hist_kernel<<<nb, 256, 0, s>>>(ids, R, E, rows, o.blockcnt, o.err);
     note_launch();
-    align_scan_kernel<<<1, SCAN_THREADS, 0, s>>>(nb, E, o.blockcnt, o);
+    // the placing CTAs copy the rows themselves when they are enough to keep
+    // most SMs busy; otherwise a separate gather spreads the copy
+    const bool copy_in_place = o.x_perm && nb >= num_sms() / 2;
+    if (copy_in_place)
+        align_place_kernel<true><<<nb, SCAN_THREADS, 0, s>>>(ids, R, k, E, rows, nb, o.blockcnt, x, d, o);
+    else
+        align_place_kernel<false><<<nb, SCAN_THREADS, 0, s>>>(ids, R, k, E, rows, nb, o.blockcnt, x, d, o);
     note_launch();
-    align_scatter_kernel<<<nb, 32, 0, s>>>(ids, R, E, rows, o.blockcnt, o);
-    note_launch();
-    if (o.x_perm) {
+    if (o.x_perm && !copy_in_place) {
         const int blocks = min(ceil_div(R, 8), 8 * num_sms());
         gather_kernel<<<blocks, 256, 0, s>>>(x, d, k, R, o);
         note_launch();

@@ -96,7 +96,8 @@ def test_route_topk_ties_and_shapes(M, T, E, k):
 # ------------------------------------------------------------------ stage 2
 @pytest.mark.parametrize("T,E,k,skew", [(8, 8, 2, False), (2, 128, 8, False), (512, 128, 8, False),
                                         (4096, 128, 8, True), (300, 1024, 7, False), (2048, 16, 1, True),
-                                        (257, 3, 3, False), (1, 1, 1, False)])
+                                        (1024, 1024, 8, True), (2600, 3, 3, False), (257, 3, 3, False),
+                                        (1, 1, 1, False)])
 def test_permute_bit_exact(M, T, E, k, skew):
     rng = np.random.default_rng(T + E + k)
     if skew:
@@ -126,6 +127,35 @@ def test_permute_reports_out_of_range_ids(M):
     assert M.get_device_error(out["ws"]) == 0  # read-and-clear
     counts = out["counts"].cpu().numpy()
     assert counts.tolist() == [1, 1, 1, 1]
+
+
+@pytest.mark.parametrize("T", [600, 2600])
+def test_permute_multiblock_skips_out_of_range_ids(M, T):
+    """Multi-block permutation (T*k > 2048 assignments; at T = 2600 the placing
+    CTAs also copy the rows): ids outside [0, E) set the range error and are
+    skipped; the valid assignments keep their stable order by expert and their
+    activation rows."""
+    rng = np.random.default_rng(T)
+    E, k, d = 64, 8, 256
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    flat = ids.reshape(-1)
+    bad = rng.choice(flat.size, size=37, replace=False)
+    flat[bad[:20]] = E + rng.integers(0, 5, size=20)
+    flat[bad[20:]] = -1 - rng.integers(0, 5, size=17)
+    x = S.f32_to_bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    out = M.permute(i32_to_dev(ids), E, x=x_to_dev(x), want_x_perm=True)
+    assert M.get_device_error(out["ws"]) == 6  # MOE_ERR_DEVICE_RANGE
+    valid = (flat >= 0) & (flat < E)
+    nv = int(valid.sum())
+    counts = out["counts"].cpu().numpy()
+    assert np.array_equal(counts, np.bincount(flat[valid], minlength=E))
+    assert np.array_equal(out["offsets"].cpu().numpy(), np.concatenate([[0], np.cumsum(counts)]))
+    a_valid = np.nonzero(valid)[0]
+    order = a_valid[np.argsort(flat[valid], kind="stable")]  # stable sort of the valid assignments
+    assert np.array_equal(out["sorted"].cpu().numpy()[:nv], order)
+    assert np.array_equal(out["inv"].cpu().numpy()[order], np.arange(nv))
+    xp = out["x_perm"].view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(xp[:nv], x[order // k])
 
 
 # ------------------------------------------------------------------ stage 3
