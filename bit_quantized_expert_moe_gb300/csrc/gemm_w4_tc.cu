@@ -9,21 +9,25 @@
 // tensor memory, where the MMA reads its A operand.
 //
 // Shapes (swap-AB: weight rows are the MMA's M, tokens its N):
-//   D[m][n] = sum_k A[m][k] * B[n][k]     M = 128 weight rows, N <= 256 tokens
+//   D[m][n] = sum_k A[m][k] * B[n][k]     M = 256 weight rows, N <= 256 tokens
 //   A = dequantised weights (fp16, written by the dequant warps into tensor
 //       memory: lane = row, a 32-bit column = two consecutive K elements)
 //   B = activation rows of one expert segment (fp16, TMA, SW128 K-major)
-// Shared memory then carries only B, the packed codes and the scales: per
-// 64-K stage the MMA reads 32 KB of B and TMA writes 36 KB, against 104 KB of
-// traffic with A staged in shared memory (written 16 KB, read 16 KB), which
-// bounded the stage time.
+// The GEMM runs on CTA pairs (2-SM clusters, tcgen05 cta_group::2): each CTA
+// dequantises its own 128 weight rows into its own tensor memory and loads
+// half of the token tile, one thread of the even CTA issues the pair's MMAs,
+// and each CTA drains its 128 rows of the accumulator.  Per 64-K stage an SM
+// then receives 16 KB of activations and 4 KB of codes (36 KB for one CTA
+// alone): the rate at which an SM's copies land, not the tensor pipe, bounded
+// the one-CTA stage.
 // The operands are fp16 rather than bf16: bf16 activations convert to fp16
 // exactly inside fp16's range (values outside set the error word), and a
 // weight is q s - fl16(z s) rounded once to fp16, which keeps 3 more bits than
 // bf16 would.  Both operands hold K interleaved in groups of 8 (k8_interleave),
 // the order in which the dequantisation takes a packed word apart.
-// A work item is (token tile of one expert, block of 128 weight rows); a
-// persistent CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...
+// A work item is (token tile of one expert, pair of 128-row weight blocks);
+// CTA rank r of the pair takes block 2 j + r of the item's pair j.  A
+// persistent pair walks items pair, pair + pairs, ...
 //
 // gate_up: the 128 A rows of a block hold 64 gate rows and the 64 matching up
 // rows, interleaved by 16 inside each 32-lane TMEM quarter, so one thread's
@@ -32,16 +36,21 @@
 // down: 128 consecutive rows of W2; the epilogue writes y rows (fp16 for the
 // layer's own combine, bf16 when y is the caller's output).
 //
-// Warp roles (896 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
-// 2-3 idle, 4-11 dequantisation (warp w: TMEM lane quarter w % 4, half
-// (w - 4) / 4 of a stage's K), 12-27 epilogue (warp w: lane quarter w % 4,
-// every fourth 32-column block).  With one accumulator the next item's MMAs
-// wait until the epilogue has read it, so four warps per quarter cut that
-// wait.
+// Warp roles (896 threads per CTA): 0 TMA producer, 1 TMEM owner and (even
+// CTA) MMA issuer, 2-3 idle, 4-11 dequantisation (warp w: TMEM lane quarter
+// w % 4, half (w - 4) / 4 of a stage's K), 12-27 epilogue (warp w: lane
+// quarter w % 4, every fourth 32-column block).  With one accumulator the
+// next item's MMAs wait until both CTAs' epilogues have read it, so four
+// warps per quarter cut that wait.
+// Barriers: each CTA's copies land on its own full[s]; both CTAs' dequant
+// warps arrive on the even CTA's afull[s] and both epilogues on its
+// accempty; MMA completion (empty[s], accfull, done) is signalled to both
+// CTAs at once.
 // TMEM: the fp32 accumulator in columns 0..255, stage s's A in columns
-// 256 + 32 s .. + 31.
+// 256 + 32 s .. + 31 (the same columns in both CTAs).
 // Every wait is bounded in time; a timeout sets the error word, every role
-// leaves its loop, in-flight copies and MMAs are drained, TMEM is freed.
+// leaves its loop, in-flight copies and MMAs are drained, and both CTAs meet
+// before TMEM is freed.
 #include <cstdio>
 
 #include "internal.h"
@@ -50,25 +59,30 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;                  // A rows per item
+constexpr int BM = 128;                  // A rows per CTA (256 per pair)
 constexpr int BK = 64;                   // K per stage: one 128-byte swizzle row of fp16
 constexpr int BN = TILE_ROWS;            // max tokens per item (256)
-constexpr int B_BYTES = BN * BK * 2;     // 32 KB
+constexpr int B_BYTES = BN / 2 * BK * 2; // 16 KB: one CTA's half of the token tile
 constexpr int P_BYTES = BM * BK / 2;     // 4 KB of packed codes
 constexpr int STAGE_BYTES = B_BYTES + P_BYTES;
-constexpr int B_BOX_ROWS = 64;           // activation rows per TMA box (fewer, larger copies: the single producer thread issues every one)
+// A CTA's half of the token tile arrives in one copy: a box of 64 rows when
+// the half is at most 64 rows, else of 128 (an SM's copies land at a limited
+// rate of operations, not only of bytes)
+constexpr int B_BOX_ROWS = 64;
 constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
 constexpr int THREADS = 896;
 constexpr int DQ_WARP0 = 4, DQ_WARPS = 8;
 constexpr int EP_WARP0 = 12, EP_WARPS = 16;
-constexpr uint32_t TMEM_COLS = 512;      // accumulator (256 columns) + S <= 6 A stages of 32 columns
+constexpr uint32_t TMEM_COLS = 512;      // accumulator (256 columns) + S <= 8 A stages of 32 columns
 constexpr uint32_t A_COL0 = 256;         // first TMEM column of stage 0's A
 constexpr uint32_t A_STAGE_COLS = BK / 2;
+constexpr int MAX_STAGES = 8;
+constexpr size_t BAR_BYTES = 512;        // barriers (8 (3 S + 9) bytes), TMEM slot, abort flag
 
 struct TcParams {
     int E, d, f, R;
     int K;        // reduction length (d for gate_up, f for down)
-    int NFB;      // weight-row blocks per expert
+    int NFB;      // 128-row weight blocks per expert (even: taken in pairs)
     const uint16_t* wsc;   // scales [E * rows_per_expert][K/128]
     const uint16_t* wz;    // zeros
     const Tile* tiles;
@@ -82,14 +96,16 @@ struct TcParams {
 
 __host__ __device__ constexpr size_t scale_bytes(int K) { return (size_t)2 * 2 * BM * (K / 128) * 2; }
 __host__ __device__ constexpr size_t tc_smem_bytes(int S, int K) {
-    return (size_t)S * STAGE_BYTES + scale_bytes(K) + 256 + 1024;
+    return (size_t)S * STAGE_BYTES + scale_bytes(K) + BAR_BYTES + 1024;
 }
 
+// Item -> expert, token rows and this CTA's weight block (rank 0 / 1 of the pair).
 template <bool GATEUP>
 __device__ __forceinline__ void item_rows(const TcParams& p, int item, int& e, int& row0, int& nrows,
                                           int& fb) {
-    const int ti = item / p.NFB;
-    fb = item - ti * p.NFB;
+    const int npb = p.NFB >> 1;
+    const int ti = item / npb;
+    fb = 2 * (item - ti * npb) + (int)tc::cluster_ctarank();
     const Tile t = p.tiles[ti];
     e = t.expert;
     row0 = t.row0;
@@ -129,9 +145,12 @@ __device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity, u
 }
 
 template <bool GATEUP, int S>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                  TcParams p) {
+                  const __grid_constant__ CUtensorMap map_x2, TcParams p) {
+    static_assert(S <= MAX_STAGES && A_COL0 + A_STAGE_COLS * S <= TMEM_COLS, "A stages exceed tensor memory");
+    static_assert(8 * (3 * S + 9) + 8 <= BAR_BYTES, "barrier area too small");
+    static_assert(S % 2 == 0, "the MMA issuer takes stages in pairs");
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -152,18 +171,21 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = p.plan->n_tiles * p.NFB;
     const int NK = p.K / BK;
+    const uint32_t rank = tc::cluster_ctarank();
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int n_items = p.plan->n_tiles * (p.NFB >> 1);
 
     if (threadIdx.x == 0) {
+        // afull and accempty count both CTAs' warps (only the even CTA's are used)
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(bar_full + 8 * s, 1);
-            tc::mbar_init(bar_afull + 8 * s, DQ_WARPS);
+            tc::mbar_init(bar_afull + 8 * s, 2 * DQ_WARPS);
             tc::mbar_init(bar_empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(bar_accfull + 8 * b, 1);
-            tc::mbar_init(bar_accempty + 8 * b, EP_WARPS);
+            tc::mbar_init(bar_accempty + 8 * b, 2 * EP_WARPS);
         }
         tc::mbar_init(bar_done, 1);
         for (int q4 = 0; q4 < 4; ++q4) tc::mbar_init(bar_qsync + 8 * q4, 2);
@@ -171,32 +193,40 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         tc::fence_mbar_init();
     }
     if (warp == 1) {
-        tc::tmem_alloc(smem_u32((const void*)tmem_slot), TMEM_COLS);
-        tc::tmem_relinquish();
+        tc::tmem_alloc_pair(smem_u32((const void*)tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish_pair();
     }
+    // both CTAs' barriers are initialised and the tensor memory allocated
+    // before either CTA signals the other
     tc::tc_fence_before();
-    __syncthreads();
+    tc::cluster_sync();
     tc::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the even CTA's afull[0] and accempty in the cluster's shared window
+    const uint32_t afull_lead = tc::mapa_shared(bar_afull, 0), accempty_lead = tc::mapa_shared(bar_accempty, 0);
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tc::tma_prefetch_desc(&map_w);
             tc::tma_prefetch_desc(&map_x);
+            tc::tma_prefetch_desc(&map_x2);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;  // per stage: last issued phase parity
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            for (int item = pair; ok && item < n_items; item += npairs) {
                 int e, row0, nrows, fb;
                 item_rows<GATEUP>(p, item, e, row0, nrows, fb);
-                const int nbox = ceil_div(nrows, B_BOX_ROWS);
+                // this CTA's half of the MMA's N (nrows rounded up to 16)
+                const int half = ceil_div(nrows, 16) * 8;
+                const int brow0 = row0 + (int)rank * half;
+                const bool big = half > B_BOX_ROWS;
                 const int wrow_a = e * p.d + fb * BM;  // down: first weight row of the block
                 for (int kc = 0; kc < NK; ++kc) {
                     if (!tc::mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.err)) { ok = false; break; }
                     const uint32_t fbar = bar_full + 8 * stage;
-                    tc::mbar_arrive_expect_tx(fbar, P_BYTES + nbox * B_BOX_BYTES);
+                    tc::mbar_arrive_expect_tx(fbar, P_BYTES + (big ? 2 : 1) * B_BOX_BYTES);
                     const uint32_t dp = sP + stage * P_BYTES;
                     // the stage's 128 rows of codes in one box: gate_up's 64 gate and
                     // 64 up rows (3D map over the expert halves), down's 128 rows
@@ -205,8 +235,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                     else
                         tc::tma_load_2d(dp, &map_w, fbar, kc * (BK / 8), wrow_a);
                     const uint32_t db = sB + stage * B_BYTES;
-                    for (int b = 0; b < nbox; ++b)
-                        tc::tma_load_2d(db + b * B_BOX_BYTES, &map_x, fbar, kc * BK, row0 + b * B_BOX_ROWS);
+                    tc::tma_load_2d(db, big ? &map_x2 : &map_x, fbar, kc * BK, brow0);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) { stage = 0; phase ^= 1; }
@@ -217,43 +246,60 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 if (issued_mask >> s & 1u) mbar_drain_wait(bar_full + 8 * s, (issued_phase >> s) & 1u, p.err);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // -------------------------------------- MMA issuer (even CTA of the pair)
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int ic = 0;
-            bool ok = true, any = false;
-            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+            bool ok = true;
+            for (int item = pair; ok && item < n_items; item += npairs, ++ic) {
                 int e, row0, nrows, fb;
                 item_rows<GATEUP>(p, item, e, row0, nrows, fb);
                 const int N = ceil_div(nrows, 16) * 16;
-                const uint32_t idesc = tc::idesc_f16_f32(BM, N);
+                const uint32_t idesc = tc::idesc_f16_f32(2 * BM, N);
                 const uint32_t aph = ic & 1;
-                if (!tc::mbar_wait(bar_accempty, aph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                // both CTAs' epilogues have read the accumulator
+                if (!tc::mbar_wait_cluster(bar_accempty, aph ^ 1, abort_flag, p.err)) { ok = false; break; }
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem_base;
-                for (int kc = 0; kc < NK; ++kc) {
-                    if (!tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err) ||
-                        !tc::mbar_wait(bar_afull + 8 * stage, phase, abort_flag, p.err)) { ok = false; break; }
+                // Stages go in pairs (S and NK are even, so a pair never
+                // wraps): one wait for 8 MMAs.  Any shared-memory access
+                // that gates the MMAs holds their issue back ~200 cycles,
+                // which at small N is longer than 4 MMAs run.
+                for (int kc = 0; kc < NK; kc += 2) {
+                    // both CTAs' A of both stages are in tensor memory, which
+                    // also means both CTAs' copies of the stages have landed
+                    const uint32_t f0 = bar_afull + 8 * stage, f1 = f0 + 8;
+                    const bool r0 = tc::mbar_test_cluster(f0, phase), r1 = tc::mbar_test_cluster(f1, phase);
+                    if (!(r0 && r1) && (!tc::mbar_wait_cluster(f0, phase, abort_flag, p.err) ||
+                                        !tc::mbar_wait_cluster(f1, phase, abort_flag, p.err))) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t a0 = tmem_base + A_COL0 + A_STAGE_COLS * stage, b0 = sB + stage * B_BYTES;
 #pragma unroll
-                    for (int ks = 0; ks < BK / 16; ++ks) {
-                        tc::mma_f16_tmem_a(d_tmem, a0 + 8 * ks, tc::sw128_kmajor_desc(b0 + ks * 32), idesc,
-                                           (kc | ks) != 0);
+                    for (int h = 0; h < 2; ++h) {
+                        const int st = stage + h;
+                        const uint32_t a0 = tmem_base + A_COL0 + A_STAGE_COLS * st, b0 = sB + st * B_BYTES;
+#pragma unroll
+                        for (int ks = 0; ks < BK / 16; ++ks) {
+                            tc::mma_f16_tmem_a_pair(d_tmem, a0 + 8 * ks, tc::sw128_kmajor_desc(b0 + ks * 32), idesc,
+                                                    ((kc + h) | ks) != 0);
+                        }
+                        tc::mma_commit_pair(bar_empty + 8 * st);
                     }
-                    tc::mma_commit(bar_empty + 8 * stage);
-                    any = true;
-                    if (++stage == S) { stage = 0; phase ^= 1; }
+                    stage += 2;
+                    if (stage == S) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                tc::mma_commit(bar_accfull);
+                tc::mma_commit_pair(bar_accfull);
             }
-            // drain: all issued MMAs complete before TMEM is released
-            if (any) {
-                tc::mma_commit(bar_done);
+            // drain: every issued MMA completes (in both CTAs) before TMEM is released
+            if (pair < n_items) {
+                tc::mma_commit_pair(bar_done);
                 mbar_drain_wait(bar_done, 0, p.err);
             }
+        } else if (lane == 0 && pair < n_items) {
+            // odd CTA: its tensor and shared memory stay in use until the
+            // even CTA's last MMA has completed
+            mbar_drain_wait(bar_done, 0, p.err);
         }
     } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + DQ_WARPS) {
         // ------------------------------------------------------ dequantisers
@@ -296,13 +342,13 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         uint32_t phase = 0;
         int ic = 0;
         bool ok = true;
-        if ((int)blockIdx.x < n_items) prefetch_scales(blockIdx.x, 0);
+        if (pair < n_items) prefetch_scales(pair, 0);
         cp_async_commit();
-        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+        for (int item = pair; ok && item < n_items; item += npairs, ++ic) {
             const int sbuf = ic & 1;
             // both warps are done with the buffer the next prefetch overwrites
             if (!quarter_sync()) break;
-            if (item + (int)gridDim.x < n_items) prefetch_scales(item + gridDim.x, sbuf ^ 1);
+            if (item + npairs < n_items) prefetch_scales(item + npairs, sbuf ^ 1);
             cp_async_commit();
             cp_async_wait<1>();
             // both warps' copies of this item's scales and zeros have landed
@@ -340,7 +386,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar_afull + 8 * stage);
+                if (lane == 0) tc::mbar_arrive_cluster(afull_lead + 8 * stage);
                 if (++stage == S) { stage = 0; phase ^= 1; }
             }
         }
@@ -350,7 +396,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         const int q = warp & 3;                 // TMEM lane quarter
         const int eh = (warp - EP_WARP0) >> 2;  // column blocks eh, eh + EP_WARPS / 4, ...
         int ic = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ic) {
+        for (int item = pair; item < n_items; item += npairs, ++ic) {
             int e, row0, nrows, fb;
             item_rows<GATEUP>(p, item, e, row0, nrows, fb);
             const uint32_t aph = ic & 1;
@@ -369,7 +415,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                     // every column read: the MMA warp may start the next item
                     tc::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(bar_accempty);
+                    if (lane == 0) tc::mbar_arrive_cluster(accempty_lead);
                 }
                 // out-of-range fp16 values are collected per column block and
                 // reported once (a branch per element costs more than the math)
@@ -424,16 +470,19 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             if (last < eh) {
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar_accempty);
+                if (lane == 0) tc::mbar_arrive_cluster(accempty_lead);
             }
         }
     }
 
+    // neither CTA frees its tensor memory or exits while the other may still
+    // signal its barriers or use its memory
+    __syncwarp();
     tc::tc_fence_before();
-    __syncthreads();
+    tc::cluster_sync();
     if (warp == 1) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem_base, TMEM_COLS);
+        tc::tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -469,13 +518,14 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* 
 
 constexpr size_t TC_SMEM_LIMIT = 232448;
 
-// Stages for a reduction length: as many as fit (4 .. 6).  A stage must be
-// refilled while the MMAs of the stages ahead of it run: the copy latency
-// (about a microsecond) plus the dequantisation has to fit in S - 1 stages'
-// MMA time, so deeper rings keep the tensor pipe fed.
+// Stages for a reduction length: 8 (all the A slots tensor memory holds
+// beside the accumulator) when they fit in shared memory, else 6 or 4.  A
+// stage must be refilled while the MMAs of the stages ahead of it run: the
+// copy latency (about a microsecond) plus the dequantisation has to fit in
+// S - 1 stages' MMA time, so deeper rings keep the tensor pipe fed.
 int tc_stages(int K) {
-    for (int st = 6; st > 4; --st)
-        if (tc_smem_bytes(st, K) <= TC_SMEM_LIMIT) return st;
+    if (tc_smem_bytes(MAX_STAGES, K) <= TC_SMEM_LIMIT) return MAX_STAGES;
+    if (tc_smem_bytes(6, K) <= TC_SMEM_LIMIT) return 6;
     return 4;
 }
 
@@ -499,7 +549,7 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
     p.err = in.err;
 
     const uint64_t rows_w = (uint64_t)E * (GATEUP ? 2 * (uint64_t)f : (uint64_t)d);
-    CUtensorMap map_w, map_x;
+    CUtensorMap map_w, map_x, map_x2;
     if (GATEUP) {
         // codes as [expert * 2 + (gate, up)][feature][K / 8 words]: box = 8 words
         // of 64 features of both halves
@@ -516,7 +566,9 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
         return cudaErrorInvalidValue;
     }
     if (!make_map(&map_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, GATEUP ? in.x16 : in.h16, (uint64_t)p.K,
-                  (uint64_t)R, BK, B_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
+                  (uint64_t)R, BK, B_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&map_x2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, GATEUP ? in.x16 : in.h16, (uint64_t)p.K,
+                  (uint64_t)R, BK, 2 * B_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
     const size_t smem = tc_smem_bytes(S, p.K);
@@ -527,9 +579,23 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int max_items = tc_max_tiles(R, E) * p.NFB;
-    const int grid = std::max(1, std::min(num_sms(), max_items));
-    tc_grouped_kernel<GATEUP, S><<<grid, THREADS, smem, s>>>(map_w, map_x, p);
+    // one CTA pair per pair of SMs that can hold one (clusters of 2 SMs)
+    static int max_pairs = 0;
+    if (max_pairs == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = smem;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, tc_grouped_kernel<GATEUP, S>, &cfg) != cudaSuccess || nc < 1) {
+            (void)cudaGetLastError();
+            nc = num_sms() / 2;
+        }
+        max_pairs = std::max(1, nc);
+    }
+    const int max_items = tc_max_tiles(R, E) * (p.NFB / 2);
+    const int grid = 2 * std::max(1, std::min(max_pairs, max_items));
+    tc_grouped_kernel<GATEUP, S><<<grid, THREADS, smem, s>>>(map_w, map_x, map_x2, p);
     note_launch();
     return cudaGetLastError();
 }
@@ -589,8 +655,8 @@ bool tc_supported(int E, int d, int f) {
 cudaError_t launch_tc_gateup(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
     switch (tc_stages(d)) {
+        case MAX_STAGES: return launch_impl<true, MAX_STAGES>(E, d, f, R, in, s);
         case 6: return launch_impl<true, 6>(E, d, f, R, in, s);
-        case 5: return launch_impl<true, 5>(E, d, f, R, in, s);
         default: return launch_impl<true, 4>(E, d, f, R, in, s);
     }
 }
@@ -598,8 +664,8 @@ cudaError_t launch_tc_gateup(int E, int d, int f, int R, const TcIn& in, cudaStr
 cudaError_t launch_tc_down(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
     switch (tc_stages(f)) {
+        case MAX_STAGES: return launch_impl<false, MAX_STAGES>(E, d, f, R, in, s);
         case 6: return launch_impl<false, 6>(E, d, f, R, in, s);
-        case 5: return launch_impl<false, 5>(E, d, f, R, in, s);
         default: return launch_impl<false, 4>(E, d, f, R, in, s);
     }
 }

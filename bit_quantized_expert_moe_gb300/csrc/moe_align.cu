@@ -74,18 +74,66 @@ __device__ void emit_plan(int cnt, int e, int E, int32_t* counts, int32_t* offse
     int n_uniq;
     const int upos = block_exclusive_scan(has, n_uniq);
     if (has && uniq) uniq[upos] = e;
-    // token tiles of at most TILE_ROWS rows
-    const int nt = live ? ceil_div(c, TILE_ROWS) : 0;
-    int n_tiles;
-    const int tpos = block_exclusive_scan(nt, n_tiles);
+    // Token tiles of at most TILE_ROWS rows: first every expert's full tiles
+    // in expert order, then each expert's last partial tile, largest first
+    // (classes of 16 rows, the MMA's N step; expert order inside a class).
+    // The grouped GEMM hands tiles to its CTA pairs round-robin, and a tile's
+    // cost grows with its rows: this order ends the list with the cheapest
+    // tiles and spreads the expensive ones evenly over the pairs.
+    if (!tiles && !plan) return;  // the same for every thread of the block
+    const int nfull = live ? c / TILE_ROWS : 0;
+    const int rem = live ? c - nfull * TILE_ROWS : 0;
+    int n_full;
+    const int fpos = block_exclusive_scan(nfull, n_full);
+    constexpr int NCLS = TILE_ROWS / 16;
+    __shared__ int cls_cnt[SCAN_THREADS / 32][NCLS + 1];  // per warp, per class: count, then prefix
+    __shared__ int cls_base[NCLS + 1];
+    __shared__ int s_n_tiles;
+    const int cls = rem > 0 ? ceil_div(rem, 16) : 0;      // 1..NCLS, 0: no partial tile
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < (SCAN_THREADS / 32) * (NCLS + 1); i += SCAN_THREADS) (&cls_cnt[0][0])[i] = 0;
+    __syncthreads();
+    const uint32_t peers = __match_any_sync(0xffffffffu, cls);
+    const int lane_rank = __popc(peers & ((1u << lane) - 1u));
+    if (lane_rank == 0) cls_cnt[wid][cls] = __popc(peers);
+    __syncthreads();
+    if (threadIdx.x <= NCLS) {
+        int run = 0;
+        for (int w = 0; w < SCAN_THREADS / 32; ++w) {
+            const int v = cls_cnt[w][threadIdx.x];
+            cls_cnt[w][threadIdx.x] = run;
+            run += v;
+        }
+        cls_base[threadIdx.x] = run;  // class total for now
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int b = n_full;
+        for (int k = NCLS; k >= 1; --k) {
+            const int tot = cls_base[k];
+            cls_base[k] = b;
+            b += tot;
+        }
+        s_n_tiles = b;
+    }
+    __syncthreads();
+    const int n_tiles = s_n_tiles;
     if (tiles) {
-        for (int i = 0; i < nt; ++i) {
+        for (int i = 0; i < nfull; ++i) {
             Tile tl;
             tl.expert = e;
             tl.row0 = off + i * TILE_ROWS;
-            tl.nrows = min(TILE_ROWS, c - i * TILE_ROWS);
+            tl.nrows = TILE_ROWS;
             tl.pad = 0;
-            tiles[tpos + i] = tl;
+            tiles[fpos + i] = tl;
+        }
+        if (cls > 0) {
+            Tile tl;
+            tl.expert = e;
+            tl.row0 = off + nfull * TILE_ROWS;
+            tl.nrows = rem;
+            tl.pad = 0;
+            tiles[cls_base[cls] + cls_cnt[wid][cls] + lane_rank] = tl;
         }
     }
     if (threadIdx.x == 0 && plan) {
