@@ -77,6 +77,7 @@ constexpr uint32_t TMEM_COLS = 512;      // accumulator (256 columns) + S <= 8 A
 constexpr uint32_t A_COL0 = 256;         // first TMEM column of stage 0's A
 constexpr uint32_t A_STAGE_COLS = BK / 2;
 constexpr int MAX_STAGES = 8;
+constexpr uint32_t SPLIT_N = BN / 2;     // tiles of at most this many tokens split K between two MMA issuers
 constexpr size_t BAR_BYTES = 512;        // barriers (8 (3 S + 9) bytes), TMEM slot, abort flag
 
 struct TcParams {
@@ -150,7 +151,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                   const __grid_constant__ CUtensorMap map_x2, TcParams p) {
     static_assert(S <= MAX_STAGES && A_COL0 + A_STAGE_COLS * S <= TMEM_COLS, "A stages exceed tensor memory");
     static_assert(8 * (3 * S + 9) + 8 <= BAR_BYTES, "barrier area too small");
-    static_assert(S % 2 == 0, "the MMA issuer takes stages in pairs");
+    static_assert(S % 2 == 0, "the MMA issuers take stages in pairs");
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -183,11 +184,12 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             tc::mbar_init(bar_afull + 8 * s, 2 * DQ_WARPS);
             tc::mbar_init(bar_empty + 8 * s, 1);
         }
+        // accfull and done: one commit from each of the two MMA issuers
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(bar_accfull + 8 * b, 1);
+            tc::mbar_init(bar_accfull + 8 * b, 2);
             tc::mbar_init(bar_accempty + 8 * b, 2 * EP_WARPS);
         }
-        tc::mbar_init(bar_done, 1);
+        tc::mbar_init(bar_done, 2);
         for (int q4 = 0; q4 < 4; ++q4) tc::mbar_init(bar_qsync + 8 * q4, 2);
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -245,48 +247,53 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             for (int s = 0; s < S; ++s)
                 if (issued_mask >> s & 1u) mbar_drain_wait(bar_full + 8 * s, (issued_phase >> s) & 1u, p.err);
         }
-    } else if (warp == 1) {
-        // -------------------------------------- MMA issuer (even CTA of the pair)
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------- MMA issuers (even CTA of the pair)
+        // Issuer 0 (warp 1) takes every stage of a tile of more than 128
+        // tokens.  A tile of at most 128 tokens splits its K between the two
+        // issuers, alternate stage pairs each, into accumulators in columns
+        // 0.. and 128.. that the epilogue adds: at small N the issue of the
+        // MMAs, not the tensor pipe, bounds a stage, and two issuers double it.
+        const int iss = warp - 1;
         if (lane == 0 && rank == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
             int ic = 0;
             bool ok = true;
-            for (int item = pair; ok && item < n_items; item += npairs, ++ic) {
+            for (int item = pair, g = 0; ok && item < n_items; item += npairs, ++ic, g += NK) {
                 int e, row0, nrows, fb;
                 item_rows<GATEUP>(p, item, e, row0, nrows, fb);
                 const int N = ceil_div(nrows, 16) * 16;
+                const bool split = N <= SPLIT_N;
                 const uint32_t idesc = tc::idesc_f16_f32(2 * BM, N);
-                const uint32_t aph = ic & 1;
                 // both CTAs' epilogues have read the accumulator
-                if (!tc::mbar_wait_cluster(bar_accempty, aph ^ 1, abort_flag, p.err)) { ok = false; break; }
+                if (!tc::mbar_wait_cluster(bar_accempty, (ic & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
                 tc::tc_fence_after();
-                const uint32_t d_tmem = tmem_base;
-                // Stages go in pairs (S and NK are even, so a pair never
-                // wraps): one wait for 8 MMAs.  Any shared-memory access
-                // that gates the MMAs holds their issue back ~200 cycles,
-                // which at small N is longer than 4 MMAs run.
-                for (int kc = 0; kc < NK; kc += 2) {
-                    // both CTAs' A of both stages are in tensor memory, which
-                    // also means both CTAs' copies of the stages have landed
-                    const uint32_t f0 = bar_afull + 8 * stage, f1 = f0 + 8;
-                    const bool r0 = tc::mbar_test_cluster(f0, phase), r1 = tc::mbar_test_cluster(f1, phase);
-                    if (!(r0 && r1) && (!tc::mbar_wait_cluster(f0, phase, abort_flag, p.err) ||
-                                        !tc::mbar_wait_cluster(f1, phase, abort_flag, p.err))) { ok = false; break; }
-                    tc::tc_fence_after();
+                if (split || iss == 0) {
+                    const uint32_t d_tmem = tmem_base + (split ? SPLIT_N * (uint32_t)iss : 0u);
+                    // Stages go in pairs (S and NK are multiples of 2 and 4, so a
+                    // pair never wraps): one wait for 8 MMAs.
+                    for (int kc = split ? 2 * iss : 0; kc < NK; kc += split ? 4 : 2) {
+                        const int gs = g + kc, stage = gs % S;
+                        const uint32_t phase = (uint32_t)(gs / S) & 1u;
+                        // both CTAs' A of both stages are in tensor memory, which
+                        // also means both CTAs' copies of the stages have landed
+                        const uint32_t f0 = bar_afull + 8 * stage, f1 = f0 + 8;
+                        const bool r0 = tc::mbar_test_cluster(f0, phase), r1 = tc::mbar_test_cluster(f1, phase);
+                        if (!(r0 && r1) && (!tc::mbar_wait_cluster(f0, phase, abort_flag, p.err) ||
+                                            !tc::mbar_wait_cluster(f1, phase, abort_flag, p.err))) { ok = false; break; }
+                        tc::tc_fence_after();
+                        const bool first = kc < 2 || (split && kc < 4);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int st = stage + h;
-                        const uint32_t a0 = tmem_base + A_COL0 + A_STAGE_COLS * st, b0 = sB + st * B_BYTES;
+                        for (int h = 0; h < 2; ++h) {
+                            const int st = stage + h;
+                            const uint32_t a0 = tmem_base + A_COL0 + A_STAGE_COLS * st, b0 = sB + st * B_BYTES;
 #pragma unroll
-                        for (int ks = 0; ks < BK / 16; ++ks) {
-                            tc::mma_f16_tmem_a_pair(d_tmem, a0 + 8 * ks, tc::sw128_kmajor_desc(b0 + ks * 32), idesc,
-                                                    ((kc + h) | ks) != 0);
+                            for (int ks = 0; ks < BK / 16; ++ks) {
+                                tc::mma_f16_tmem_a_pair(d_tmem, a0 + 8 * ks, tc::sw128_kmajor_desc(b0 + ks * 32), idesc,
+                                                        !(first && h == 0 && ks == 0));
+                            }
+                            tc::mma_commit_pair(bar_empty + 8 * st);
                         }
-                        tc::mma_commit_pair(bar_empty + 8 * st);
                     }
-                    stage += 2;
-                    if (stage == S) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
                 tc::mma_commit_pair(bar_accfull);
@@ -296,9 +303,9 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 tc::mma_commit_pair(bar_done);
                 mbar_drain_wait(bar_done, 0, p.err);
             }
-        } else if (lane == 0 && pair < n_items) {
+        } else if (lane == 0 && iss == 0 && pair < n_items) {
             // odd CTA: its tensor and shared memory stay in use until the
-            // even CTA's last MMA has completed
+            // even CTA's last MMAs have completed
             mbar_drain_wait(bar_done, 0, p.err);
         }
     } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + DQ_WARPS) {
@@ -353,41 +360,54 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             cp_async_wait<1>();
             // both warps' copies of this item's scales and zeros have landed
             if (!quarter_sync()) break;
-            uint32_t s2 = 0, nzs2 = 0;  // as f16x2: (s, s) and (-fl16(z s), -fl16(z s))
-            for (int kc = 0; kc < NK; ++kc) {
-                ok = tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err);
+            // Stages go in pairs (S and NK are even): both stages of a pair
+            // lie in one scale group of 128 K, and taking them together
+            // overlaps one stage's latencies (wait, load, store) with the
+            // other's.
+            for (int kc = 0; kc < NK; kc += 2) {
+                ok = tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err) &&
+                     tc::mbar_wait(bar_full + 8 * (stage + 1), phase, abort_flag, p.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if ((kc & 1) == 0) {
-                    const size_t si = ((size_t)sbuf * BM + r) * G + (kc >> 1);
-                    const uint32_t sb = sScale[si];
-                    const float zs = half_bits_to_float((uint16_t)sb) * half_bits_to_float(sZero[si]);
-                    s2 = sb * 0x10001u;
-                    nzs2 = (uint32_t)float_to_f16_bits(-zs) * 0x10001u;
-                }
-                // this row's 4 words of the half: codes 32 hk .. 32 hk + 31 of the stage
-                const uint4 pw = *reinterpret_cast<const uint4*>(gbase + (sP - base) + stage * P_BYTES + prow * 32 + hk * 16);
-                const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
-                uint32_t o[16];
+                // as f16x2: (s, s) and (-fl16(z s), -fl16(z s)) of this row's group kc / 2
+                const size_t si = ((size_t)sbuf * BM + r) * G + (kc >> 1);
+                const uint32_t sb = sScale[si];
+                const float zs = half_bits_to_float((uint16_t)sb) * half_bits_to_float(sZero[si]);
+                const uint32_t s2 = sb * 0x10001u;
+                const uint32_t nzs2 = (uint32_t)float_to_f16_bits(-zs) * 0x10001u;
+                // this row's 4 words of the half in each stage: codes 32 hk .. 32 hk + 31
+                uint4 pw[2];
 #pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-                    // the 8 codes of one word in the operand order (k0,k4)
-                    // (k1,k5) (k2,k6) (k3,k7): masking a nibble into the
-                    // mantissa of 1024.0 (bits 0-3) or 64.0 (bits 4-7) gives
-                    // 1024 + q or 64 + q exactly, minus the base gives q
-                    // exactly, and one fma gives q s - fl16(z s) rounded once
-                    const uint32_t word = words[wi], ws = word >> 8;
-                    o[4 * wi + 0] = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x000F000Fu, 0x64006400u), 0x64006400u), s2, nzs2);
-                    o[4 * wi + 1] = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x00F000F0u, 0x54005400u), 0x54005400u), s2, nzs2);
-                    o[4 * wi + 2] = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x000F000Fu, 0x64006400u), 0x64006400u), s2, nzs2);
-                    o[4 * wi + 3] = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x00F000F0u, 0x54005400u), 0x54005400u), s2, nzs2);
+                for (int h = 0; h < 2; ++h)
+                    pw[h] = *reinterpret_cast<const uint4*>(gbase + (sP - base) + (stage + h) * P_BYTES + prow * 32 + hk * 16);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t words[4] = {pw[h].x, pw[h].y, pw[h].z, pw[h].w};
+                    uint32_t o[16];
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        // the 8 codes of one word in the operand order (k0,k4)
+                        // (k1,k5) (k2,k6) (k3,k7): masking a nibble into the
+                        // mantissa of 1024.0 (bits 0-3) or 64.0 (bits 4-7) gives
+                        // 1024 + q or 64 + q exactly, minus the base gives q
+                        // exactly, and one fma gives q s - fl16(z s) rounded once
+                        const uint32_t word = words[wi], ws = word >> 8;
+                        o[4 * wi + 0] = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x000F000Fu, 0x64006400u), 0x64006400u), s2, nzs2);
+                        o[4 * wi + 1] = hfma2_u32(hsub2_u32(lop_mask_or(word, 0x00F000F0u, 0x54005400u), 0x54005400u), s2, nzs2);
+                        o[4 * wi + 2] = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x000F000Fu, 0x64006400u), 0x64006400u), s2, nzs2);
+                        o[4 * wi + 3] = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x00F000F0u, 0x54005400u), 0x54005400u), s2, nzs2);
+                    }
+                    tc::tmem_st_32x32b_x16(tmem_base + t_lane + A_COL0 + A_STAGE_COLS * (stage + h) + 16 * hk, o);
                 }
-                tc::tmem_st_32x32b_x16(tmem_base + t_lane + A_COL0 + A_STAGE_COLS * stage + 16 * hk, o);
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive_cluster(afull_lead + 8 * stage);
-                if (++stage == S) { stage = 0; phase ^= 1; }
+                if (lane == 0) {
+                    tc::mbar_arrive_cluster(afull_lead + 8 * stage);
+                    tc::mbar_arrive_cluster(afull_lead + 8 * (stage + 1));
+                }
+                stage += 2;
+                if (stage == S) { stage = 0; phase ^= 1; }
             }
         }
         cp_async_wait<0>();
@@ -404,13 +424,27 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::tc_fence_after();
             const int ncb = ceil_div(nrows, 32);
+            // K split between the two MMA issuers: the sum of two accumulators
+            const bool split = ceil_div(nrows, 16) * 16 <= SPLIT_N;
             // this warp's last block (< eh: none)
             constexpr int EP_STEP = EP_WARPS / 4;
             const int last = ncb - 1 < eh ? -1 : eh + EP_STEP * ((ncb - 1 - eh) / EP_STEP);
             for (int cb = eh; cb < ncb; cb += EP_STEP) {
                 uint32_t v[32];
-                tc::tmem_ld_32x32b_x32(tmem_base + cb * 32 + ((uint32_t)(32 * q) << 16), v);
+                const uint32_t ta = tmem_base + cb * 32 + ((uint32_t)(32 * q) << 16);
+                tc::tmem_ld_32x32b_x32(ta, v);
                 tc::tmem_ld_wait();
+                if (split) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t t[16];
+                        tc::tmem_ld_32x32b_x16(ta + SPLIT_N + 16 * hh, t);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            v[16 * hh + j] = __float_as_uint(__uint_as_float(v[16 * hh + j]) + __uint_as_float(t[j]));
+                    }
+                }
                 if (cb == last) {
                     // every column read: the MMA warp may start the next item
                     tc::tc_fence_before();
