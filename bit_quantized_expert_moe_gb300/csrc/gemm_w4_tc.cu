@@ -20,6 +20,10 @@
 // then receives 16 KB of activations and 4 KB of codes (36 KB for one CTA
 // alone): the rate at which an SM's copies land, not the tensor pipe, bounded
 // the one-CTA stage.
+// The pipeline moves in units of 128 K (two 64-K sub-stages, one scale
+// group): one barrier round, one copy of codes and one wait per unit.  The
+// shared-memory ring holds one unit more than tensor memory holds A units, so
+// the copies are issued one unit earlier.
 // The operands are fp16 rather than bf16: bf16 activations convert to fp16
 // exactly inside fp16's range (values outside set the error word), and a
 // weight is q s - fl16(z s) rounded once to fp16, which keeps 3 more bits than
@@ -38,16 +42,16 @@
 //
 // Warp roles (896 threads per CTA): 0 TMA producer, 1 TMEM owner and (even
 // CTA) MMA issuer, 2-3 idle, 4-11 dequantisation (warp w: TMEM lane quarter
-// w % 4, half (w - 4) / 4 of a stage's K), 12-27 epilogue (warp w: lane
+// w % 4, half (w - 4) / 4 of a sub-stage's K), 12-27 epilogue (warp w: lane
 // quarter w % 4, every fourth 32-column block).  With one accumulator the
 // next item's MMAs wait until both CTAs' epilogues have read it, so four
 // warps per quarter cut that wait.
-// Barriers: each CTA's copies land on its own full[s]; both CTAs' dequant
-// warps arrive on the even CTA's afull[s] and both epilogues on its
-// accempty; MMA completion (empty[s], accfull, done) is signalled to both
-// CTAs at once.
-// TMEM: the fp32 accumulator in columns 0..255, stage s's A in columns
-// 256 + 32 s .. + 31 (the same columns in both CTAs).
+// Barriers: each CTA's copies land on its own full[u]; both CTAs' dequant
+// warps arrive on the even CTA's afull[a] and both epilogues on its
+// accempty; MMA completion (empty[u], aempty[a], accfull, done) is signalled
+// to both CTAs at once.
+// TMEM: the fp32 accumulator in columns 0..255, A unit a in columns
+// 256 + 64 a .. + 63 (the same columns in both CTAs).
 // Every wait is bounded in time; a timeout sets the error word, every role
 // leaves its loop, in-flight copies and MMAs are drained, and both CTAs meet
 // before TMEM is freed.
@@ -60,11 +64,12 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;                  // A rows per CTA (256 per pair)
-constexpr int BK = 64;                   // K per stage: one 128-byte swizzle row of fp16
+constexpr int BK = 64;                   // K per sub-stage: one 128-byte swizzle row of fp16
+constexpr int UK = 2 * BK;               // K per pipeline unit (= the scale group)
 constexpr int BN = TILE_ROWS;            // max tokens per item (256)
-constexpr int B_BYTES = BN / 2 * BK * 2; // 16 KB: one CTA's half of the token tile
-constexpr int P_BYTES = BM * BK / 2;     // 4 KB of packed codes
-constexpr int STAGE_BYTES = B_BYTES + P_BYTES;
+constexpr int B_BYTES = BN / 2 * BK * 2; // 16 KB: one CTA's half of the token tile, one sub-stage
+constexpr int P_BYTES = BM * UK / 2;     // 8 KB of packed codes per unit
+constexpr int UNIT_BYTES = 2 * B_BYTES + P_BYTES;
 // A CTA's half of the token tile arrives in one copy: a box of 64 rows when
 // the half is at most 64 rows, else of 128 (an SM's copies land at a limited
 // rate of operations, not only of bytes)
@@ -73,12 +78,13 @@ constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
 constexpr int THREADS = 896;
 constexpr int DQ_WARP0 = 4, DQ_WARPS = 8;
 constexpr int EP_WARP0 = 12, EP_WARPS = 16;
-constexpr uint32_t TMEM_COLS = 512;      // accumulator (256 columns) + S <= 8 A stages of 32 columns
-constexpr uint32_t A_COL0 = 256;         // first TMEM column of stage 0's A
-constexpr uint32_t A_STAGE_COLS = BK / 2;
-constexpr int MAX_STAGES = 8;
+constexpr uint32_t TMEM_COLS = 512;      // accumulator (256 columns) + 4 A units of 64 columns
+constexpr uint32_t A_COL0 = 256;         // first TMEM column of A unit 0
+constexpr uint32_t A_UNIT_COLS = UK / 2;
+constexpr int A_UNITS = 4;
+constexpr int MAX_UNITS = 6;
 constexpr uint32_t SPLIT_N = BN / 2;     // tiles of at most this many tokens split K between two MMA issuers
-constexpr size_t BAR_BYTES = 512;        // barriers (8 (3 S + 9) bytes), TMEM slot, abort flag
+constexpr size_t BAR_BYTES = 512;        // barriers (8 (2 SU + 2 A_UNITS + 9) bytes), TMEM slot, abort flag
 
 struct TcParams {
     int E, d, f, R;
@@ -96,8 +102,8 @@ struct TcParams {
 };
 
 __host__ __device__ constexpr size_t scale_bytes(int K) { return (size_t)2 * 2 * BM * (K / 128) * 2; }
-__host__ __device__ constexpr size_t tc_smem_bytes(int S, int K) {
-    return (size_t)S * STAGE_BYTES + scale_bytes(K) + BAR_BYTES + 1024;
+__host__ __device__ constexpr size_t tc_smem_bytes(int SU, int K) {
+    return (size_t)SU * UNIT_BYTES + scale_bytes(K) + BAR_BYTES + 1024;
 }
 
 // Item -> expert, token rows and this CTA's weight block (rank 0 / 1 of the pair).
@@ -125,7 +131,7 @@ __device__ __forceinline__ size_t a_global_row(const TcParams& p, int e, int fb,
     }
 }
 
-// Row of the packed-code stage buffer that holds A row r.
+// Row of a unit's packed-code buffer that holds A row r.
 template <bool GATEUP>
 __device__ __forceinline__ int a_packed_row(int r) {
     if (GATEUP) {
@@ -145,44 +151,51 @@ __device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity, u
     }
 }
 
-template <bool GATEUP, int S>
+template <bool GATEUP, int SU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                   const __grid_constant__ CUtensorMap map_x2, TcParams p) {
-    static_assert(S <= MAX_STAGES && A_COL0 + A_STAGE_COLS * S <= TMEM_COLS, "A stages exceed tensor memory");
-    static_assert(8 * (3 * S + 9) + 8 <= BAR_BYTES, "barrier area too small");
-    static_assert(S % 2 == 0, "the MMA issuers take stages in pairs");
+    static_assert(SU <= MAX_UNITS && A_COL0 + A_UNIT_COLS * A_UNITS <= TMEM_COLS, "A units exceed tensor memory");
+    constexpr int NBAR = 2 * SU + 2 * A_UNITS + 9;
+    static_assert(8 * NBAR + 8 <= BAR_BYTES, "barrier area too small");
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* gbase = smem_raw + (base - raw);
 
+    // shared memory: per unit slot two 16 KB activation sub-stages (128B-swizzled
+    // K-major), then the units' codes ([128 rows][16 words]), the scales and zeros,
+    // the barriers
     const uint32_t sB = base;
-    const uint32_t sP = base + S * B_BYTES;
+    const uint32_t sP = base + SU * 2 * B_BYTES;
     const int G = p.K / 128;
-    uint16_t* sScale = reinterpret_cast<uint16_t*>(gbase + S * STAGE_BYTES);  // [2][BM][G]
-    uint16_t* sZero = sScale + 2 * BM * G;                                     // [2][BM][G]
-    const uint32_t bars = base + S * STAGE_BYTES + (uint32_t)scale_bytes(p.K);
-    // barrier layout: full[S], afull[S], empty[S], accfull[2], accempty[2], done, qsync[4]
-    // (one accumulator: only accfull[0] and accempty[0] are used)
-    const uint32_t bar_full = bars, bar_afull = bars + 8 * S, bar_empty = bars + 16 * S;
-    const uint32_t bar_accfull = bars + 24 * S, bar_accempty = bar_accfull + 16, bar_done = bar_accempty + 16;
+    uint16_t* sScale = reinterpret_cast<uint16_t*>(gbase + SU * UNIT_BYTES);  // [2][BM][G]
+    uint16_t* sZero = sScale + 2 * BM * G;                                    // [2][BM][G]
+    const uint32_t bars = base + SU * UNIT_BYTES + (uint32_t)scale_bytes(p.K);
+    // barrier layout: full[SU], empty[SU], afull[A_UNITS], aempty[A_UNITS], accfull[2],
+    // accempty[2], done, qsync[4] (one accumulator: only accfull[0] and accempty[0] are used)
+    const uint32_t bar_full = bars, bar_empty = bars + 8 * SU, bar_afull = bars + 16 * SU;
+    const uint32_t bar_aempty = bar_afull + 8 * A_UNITS, bar_accfull = bar_aempty + 8 * A_UNITS;
+    const uint32_t bar_accempty = bar_accfull + 16, bar_done = bar_accempty + 16;
     const uint32_t bar_qsync = bar_done + 8;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + S * STAGE_BYTES + scale_bytes(p.K) + 8 * (3 * S + 9));
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + SU * UNIT_BYTES + scale_bytes(p.K) + 8 * NBAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NK = p.K / BK;
+    const int NU = p.K / UK;  // units per item (even: K is a multiple of 256)
     const uint32_t rank = tc::cluster_ctarank();
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int n_items = p.plan->n_tiles * (p.NFB >> 1);
 
     if (threadIdx.x == 0) {
         // afull and accempty count both CTAs' warps (only the even CTA's are used)
-        for (int s = 0; s < S; ++s) {
-            tc::mbar_init(bar_full + 8 * s, 1);
-            tc::mbar_init(bar_afull + 8 * s, 2 * DQ_WARPS);
-            tc::mbar_init(bar_empty + 8 * s, 1);
+        for (int u = 0; u < SU; ++u) {
+            tc::mbar_init(bar_full + 8 * u, 1);
+            tc::mbar_init(bar_empty + 8 * u, 1);
+        }
+        for (int a = 0; a < A_UNITS; ++a) {
+            tc::mbar_init(bar_afull + 8 * a, 2 * DQ_WARPS);
+            tc::mbar_init(bar_aempty + 8 * a, 1);
         }
         // accfull and done: one commit from each of the two MMA issuers
         for (int b = 0; b < 2; ++b) {
@@ -213,9 +226,8 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             tc::tma_prefetch_desc(&map_w);
             tc::tma_prefetch_desc(&map_x);
             tc::tma_prefetch_desc(&map_x2);
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_phase = 0;  // per stage: last issued phase parity
+            int gu = 0;  // units issued so far
+            uint32_t issued_mask = 0, issued_phase = 0;  // per unit slot: last issued phase parity
             bool ok = true;
             for (int item = pair; ok && item < n_items; item += npairs) {
                 int e, row0, nrows, fb;
@@ -225,40 +237,43 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 const int brow0 = row0 + (int)rank * half;
                 const bool big = half > B_BOX_ROWS;
                 const int wrow_a = e * p.d + fb * BM;  // down: first weight row of the block
-                for (int kc = 0; kc < NK; ++kc) {
-                    if (!tc::mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag, p.err)) { ok = false; break; }
-                    const uint32_t fbar = bar_full + 8 * stage;
-                    tc::mbar_arrive_expect_tx(fbar, P_BYTES + (big ? 2 : 1) * B_BOX_BYTES);
-                    const uint32_t dp = sP + stage * P_BYTES;
-                    // the stage's 128 rows of codes in one box: gate_up's 64 gate and
+                for (int ku = 0; ku < NU; ++ku, ++gu) {
+                    const int u = gu % SU;
+                    const uint32_t pu = (uint32_t)(gu / SU) & 1u;
+                    if (!tc::mbar_wait(bar_empty + 8 * u, pu ^ 1, abort_flag, p.err)) { ok = false; break; }
+                    const uint32_t fbar = bar_full + 8 * u;
+                    tc::mbar_arrive_expect_tx(fbar, P_BYTES + 2 * (big ? 2 : 1) * B_BOX_BYTES);
+                    const uint32_t dp = sP + u * P_BYTES;
+                    // the unit's 128 rows of codes in one box: gate_up's 64 gate and
                     // 64 up rows (3D map over the expert halves), down's 128 rows
                     if (GATEUP)
-                        tc::tma_load_3d(dp, &map_w, fbar, kc * (BK / 8), fb * 64, 2 * e);
+                        tc::tma_load_3d(dp, &map_w, fbar, ku * (UK / 8), fb * 64, 2 * e);
                     else
-                        tc::tma_load_2d(dp, &map_w, fbar, kc * (BK / 8), wrow_a);
-                    const uint32_t db = sB + stage * B_BYTES;
-                    tc::tma_load_2d(db, big ? &map_x2 : &map_x, fbar, kc * BK, brow0);
-                    issued_mask |= 1u << stage;
-                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == S) { stage = 0; phase ^= 1; }
+                        tc::tma_load_2d(dp, &map_w, fbar, ku * (UK / 8), wrow_a);
+                    const uint32_t db = sB + u * 2 * B_BYTES;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tc::tma_load_2d(db + h * B_BYTES, big ? &map_x2 : &map_x, fbar, ku * UK + h * BK, brow0);
+                    issued_mask |= 1u << u;
+                    issued_phase = (issued_phase & ~(1u << u)) | (pu << u);
                 }
             }
-            // drain: every issued stage's copies must have landed before exit
-            for (int s = 0; s < S; ++s)
-                if (issued_mask >> s & 1u) mbar_drain_wait(bar_full + 8 * s, (issued_phase >> s) & 1u, p.err);
+            // drain: every issued unit's copies must have landed before exit
+            for (int u = 0; u < SU; ++u)
+                if (issued_mask >> u & 1u) mbar_drain_wait(bar_full + 8 * u, (issued_phase >> u) & 1u, p.err);
         }
     } else if (warp == 1 || warp == 2) {
         // ------------------------------------- MMA issuers (even CTA of the pair)
-        // Issuer 0 (warp 1) takes every stage of a tile of more than 128
+        // Issuer 0 (warp 1) takes every unit of a tile of more than 128
         // tokens.  A tile of at most 128 tokens splits its K between the two
-        // issuers, alternate stage pairs each, into accumulators in columns
-        // 0.. and 128.. that the epilogue adds: at small N the issue of the
-        // MMAs, not the tensor pipe, bounds a stage, and two issuers double it.
+        // issuers, alternate units each, into accumulators in columns 0.. and
+        // 128.. that the epilogue adds: at small N the issue of the MMAs, not
+        // the tensor pipe, bounds a unit, and two issuers double it.
         const int iss = warp - 1;
         if (lane == 0 && rank == 0) {
             int ic = 0;
             bool ok = true;
-            for (int item = pair, g = 0; ok && item < n_items; item += npairs, ++ic, g += NK) {
+            for (int item = pair, g = 0; ok && item < n_items; item += npairs, ++ic, g += NU) {
                 int e, row0, nrows, fb;
                 item_rows<GATEUP>(p, item, e, row0, nrows, fb);
                 const int N = ceil_div(nrows, 16) * 16;
@@ -269,30 +284,28 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 tc::tc_fence_after();
                 if (split || iss == 0) {
                     const uint32_t d_tmem = tmem_base + (split ? SPLIT_N * (uint32_t)iss : 0u);
-                    // Stages go in pairs (S and NK are multiples of 2 and 4, so a
-                    // pair never wraps): one wait for 8 MMAs.
-                    for (int kc = split ? 2 * iss : 0; kc < NK; kc += split ? 4 : 2) {
-                        const int gs = g + kc, stage = gs % S;
-                        const uint32_t phase = (uint32_t)(gs / S) & 1u;
-                        // both CTAs' A of both stages are in tensor memory, which
-                        // also means both CTAs' copies of the stages have landed
-                        const uint32_t f0 = bar_afull + 8 * stage, f1 = f0 + 8;
-                        const bool r0 = tc::mbar_test_cluster(f0, phase), r1 = tc::mbar_test_cluster(f1, phase);
-                        if (!(r0 && r1) && (!tc::mbar_wait_cluster(f0, phase, abort_flag, p.err) ||
-                                            !tc::mbar_wait_cluster(f1, phase, abort_flag, p.err))) { ok = false; break; }
+                    const int ku0 = split ? iss : 0;
+                    for (int ku = ku0; ku < NU; ku += split ? 2 : 1) {
+                        const int gu = g + ku, a = gu % A_UNITS, u = gu % SU;
+                        // both CTAs' A of the unit are in tensor memory, which
+                        // also means both CTAs' copies of the unit have landed
+                        if (!tc::mbar_wait_cluster(bar_afull + 8 * a, (uint32_t)(gu / A_UNITS) & 1u, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
                         tc::tc_fence_after();
-                        const bool first = kc < 2 || (split && kc < 4);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const int st = stage + h;
-                            const uint32_t a0 = tmem_base + A_COL0 + A_STAGE_COLS * st, b0 = sB + st * B_BYTES;
+                            const uint32_t a0 = tmem_base + A_COL0 + A_UNIT_COLS * a + BK / 2 * h;
+                            const uint32_t b0 = sB + u * 2 * B_BYTES + h * B_BYTES;
 #pragma unroll
                             for (int ks = 0; ks < BK / 16; ++ks) {
                                 tc::mma_f16_tmem_a_pair(d_tmem, a0 + 8 * ks, tc::sw128_kmajor_desc(b0 + ks * 32), idesc,
-                                                        !(first && h == 0 && ks == 0));
+                                                        !(ku == ku0 && h == 0 && ks == 0));
                             }
-                            tc::mma_commit_pair(bar_empty + 8 * st);
                         }
+                        tc::mma_commit_pair(bar_empty + 8 * u);
+                        tc::mma_commit_pair(bar_aempty + 8 * a);
                     }
                 }
                 if (!ok) break;
@@ -311,8 +324,8 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + DQ_WARPS) {
         // ------------------------------------------------------ dequantisers
         // Warp w owns A row r = 32 (w % 4) + lane (its TMEM lane) and half
-        // hk = (w - 4) / 4 of every stage's K: 4 packed words (32 codes) per
-        // stage, widened in registers and stored as 16 TMEM columns.  The two
+        // hk = (w - 4) / 4 of every sub-stage's K: 4 packed words (32 codes)
+        // per sub-stage, widened in registers and stored as 16 TMEM columns.  The two
         // warps of a lane quarter share its rows' scales and zeros: warp hk
         // prefetches array hk (scales, zeros) of the next item into the other
         // half of a double buffer (4-byte cp.async).  They meet on a named
@@ -345,8 +358,7 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 cp_async4(smem_u32(s_dst + ((size_t)buf * BM + rr) * G + 2 * gp), s_src + grow * G + 2 * gp);
             }
         };
-        int stage = 0;
-        uint32_t phase = 0;
+        int gu = 0;  // units consumed so far
         int ic = 0;
         bool ok = true;
         if (pair < n_items) prefetch_scales(pair, 0);
@@ -360,26 +372,25 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             cp_async_wait<1>();
             // both warps' copies of this item's scales and zeros have landed
             if (!quarter_sync()) break;
-            // Stages go in pairs (S and NK are even): both stages of a pair
-            // lie in one scale group of 128 K, and taking them together
-            // overlaps one stage's latencies (wait, load, store) with the
-            // other's.
-            for (int kc = 0; kc < NK; kc += 2) {
-                ok = tc::mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.err) &&
-                     tc::mbar_wait(bar_full + 8 * (stage + 1), phase, abort_flag, p.err);
+            for (int ku = 0; ku < NU; ++ku, ++gu) {
+                const int u = gu % SU, a = gu % A_UNITS;
+                // the unit's copies have landed and the MMAs that read A unit a
+                // the previous time have completed
+                ok = tc::mbar_wait(bar_full + 8 * u, (uint32_t)(gu / SU) & 1u, abort_flag, p.err) &&
+                     tc::mbar_wait(bar_aempty + 8 * a, ((uint32_t)(gu / A_UNITS) & 1u) ^ 1u, abort_flag, p.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                // as f16x2: (s, s) and (-fl16(z s), -fl16(z s)) of this row's group kc / 2
-                const size_t si = ((size_t)sbuf * BM + r) * G + (kc >> 1);
+                // as f16x2: (s, s) and (-fl16(z s), -fl16(z s)) of this row's group ku
+                const size_t si = ((size_t)sbuf * BM + r) * G + ku;
                 const uint32_t sb = sScale[si];
                 const float zs = half_bits_to_float((uint16_t)sb) * half_bits_to_float(sZero[si]);
                 const uint32_t s2 = sb * 0x10001u;
                 const uint32_t nzs2 = (uint32_t)float_to_f16_bits(-zs) * 0x10001u;
-                // this row's 4 words of the half in each stage: codes 32 hk .. 32 hk + 31
+                // this row's 4 words of the half in each sub-stage: codes 32 hk .. 32 hk + 31
                 uint4 pw[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    pw[h] = *reinterpret_cast<const uint4*>(gbase + (sP - base) + (stage + h) * P_BYTES + prow * 32 + hk * 16);
+                    pw[h] = *reinterpret_cast<const uint4*>(gbase + (sP - base) + u * P_BYTES + prow * (UK / 2) + h * 32 + hk * 16);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t words[4] = {pw[h].x, pw[h].y, pw[h].z, pw[h].w};
@@ -397,17 +408,12 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                         o[4 * wi + 2] = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x000F000Fu, 0x64006400u), 0x64006400u), s2, nzs2);
                         o[4 * wi + 3] = hfma2_u32(hsub2_u32(lop_mask_or(ws, 0x00F000F0u, 0x54005400u), 0x54005400u), s2, nzs2);
                     }
-                    tc::tmem_st_32x32b_x16(tmem_base + t_lane + A_COL0 + A_STAGE_COLS * (stage + h) + 16 * hk, o);
+                    tc::tmem_st_32x32b_x16(tmem_base + t_lane + A_COL0 + A_UNIT_COLS * a + BK / 2 * h + 16 * hk, o);
                 }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    tc::mbar_arrive_cluster(afull_lead + 8 * stage);
-                    tc::mbar_arrive_cluster(afull_lead + 8 * (stage + 1));
-                }
-                stage += 2;
-                if (stage == S) { stage = 0; phase ^= 1; }
+                if (lane == 0) tc::mbar_arrive_cluster(afull_lead + 8 * a);
             }
         }
         cp_async_wait<0>();
@@ -552,18 +558,14 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* 
 
 constexpr size_t TC_SMEM_LIMIT = 232448;
 
-// Stages for a reduction length: 8 (all the A slots tensor memory holds
-// beside the accumulator) when they fit in shared memory, else 6 or 4.  A
-// stage must be refilled while the MMAs of the stages ahead of it run: the
-// copy latency (about a microsecond) plus the dequantisation has to fit in
-// S - 1 stages' MMA time, so deeper rings keep the tensor pipe fed.
-int tc_stages(int K) {
-    if (tc_smem_bytes(MAX_STAGES, K) <= TC_SMEM_LIMIT) return MAX_STAGES;
-    if (tc_smem_bytes(6, K) <= TC_SMEM_LIMIT) return 6;
-    return 4;
-}
+// Units of the shared-memory ring for a reduction length: 5 when they fit
+// (one more than the A units in tensor memory), else 4.  A unit must be
+// refilled while the MMAs of the units ahead of it run: the copy latency
+// (about a microsecond) plus the dequantisation has to fit in SU - 1 units'
+// MMA time, so the deeper ring keeps the tensor pipe fed.
+int tc_units(int K) { return tc_smem_bytes(5, K) <= TC_SMEM_LIMIT ? 5 : 4; }
 
-template <bool GATEUP, int S>
+template <bool GATEUP, int SU>
 cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
     TcParams p{};
     p.E = E;
@@ -590,12 +592,12 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
         EncodeFn enc = get_encode();
         const cuuint64_t dims[3] = {(cuuint64_t)p.K / 8, (cuuint64_t)f, (cuuint64_t)E * 2};
         const cuuint64_t strides[2] = {(cuuint64_t)p.K / 2, (cuuint64_t)f * p.K / 2};
-        const cuuint32_t box[3] = {BK / 8, 64, 2}, estr[3] = {1, 1, 1};
+        const cuuint32_t box[3] = {UK / 8, 64, 2}, estr[3] = {1, 1, 1};
         if (!enc || enc(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(in.w13_q), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-    } else if (!make_map(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, in.w2_q, (uint64_t)p.K / 8, rows_w, BK / 8, BM,
+    } else if (!make_map(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, in.w2_q, (uint64_t)p.K / 8, rows_w, UK / 8, BM,
                          CU_TENSOR_MAP_SWIZZLE_NONE)) {
         return cudaErrorInvalidValue;
     }
@@ -605,10 +607,10 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
                   (uint64_t)R, BK, 2 * B_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
-    const size_t smem = tc_smem_bytes(S, p.K);
+    const size_t smem = tc_smem_bytes(SU, p.K);
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<GATEUP, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(tc_grouped_kernel<GATEUP, SU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)TC_SMEM_LIMIT);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -621,7 +623,7 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
         cfg.blockDim = dim3(THREADS);
         cfg.dynamicSmemBytes = smem;
         int nc = 0;
-        if (cudaOccupancyMaxActiveClusters(&nc, tc_grouped_kernel<GATEUP, S>, &cfg) != cudaSuccess || nc < 1) {
+        if (cudaOccupancyMaxActiveClusters(&nc, tc_grouped_kernel<GATEUP, SU>, &cfg) != cudaSuccess || nc < 1) {
             (void)cudaGetLastError();
             nc = num_sms() / 2;
         }
@@ -629,7 +631,7 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
     }
     const int max_items = tc_max_tiles(R, E) * (p.NFB / 2);
     const int grid = 2 * std::max(1, std::min(max_pairs, max_items));
-    tc_grouped_kernel<GATEUP, S><<<grid, THREADS, smem, s>>>(map_w, map_x, map_x2, p);
+    tc_grouped_kernel<GATEUP, SU><<<grid, THREADS, smem, s>>>(map_w, map_x, map_x2, p);
     note_launch();
     return cudaGetLastError();
 }
@@ -688,20 +690,12 @@ bool tc_supported(int E, int d, int f) {
 
 cudaError_t launch_tc_gateup(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
-    switch (tc_stages(d)) {
-        case MAX_STAGES: return launch_impl<true, MAX_STAGES>(E, d, f, R, in, s);
-        case 6: return launch_impl<true, 6>(E, d, f, R, in, s);
-        default: return launch_impl<true, 4>(E, d, f, R, in, s);
-    }
+    return tc_units(d) == 5 ? launch_impl<true, 5>(E, d, f, R, in, s) : launch_impl<true, 4>(E, d, f, R, in, s);
 }
 
 cudaError_t launch_tc_down(int E, int d, int f, int R, const TcIn& in, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
-    switch (tc_stages(f)) {
-        case MAX_STAGES: return launch_impl<false, MAX_STAGES>(E, d, f, R, in, s);
-        case 6: return launch_impl<false, 6>(E, d, f, R, in, s);
-        default: return launch_impl<false, 4>(E, d, f, R, in, s);
-    }
+    return tc_units(f) == 5 ? launch_impl<false, 5>(E, d, f, R, in, s) : launch_impl<false, 4>(E, d, f, R, in, s);
 }
 
 }  // namespace moe
