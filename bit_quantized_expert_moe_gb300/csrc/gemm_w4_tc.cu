@@ -251,9 +251,10 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                     else
                         tc::tma_load_2d(dp, &map_w, fbar, ku * (UK / 8), wrow_a);
                     const uint32_t db = sB + u * 2 * B_BYTES;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tc::tma_load_2d(db + h * B_BYTES, big ? &map_x2 : &map_x, fbar, ku * UK + h * BK, brow0);
+                    // both sub-stages of the activation half in one box of a 3D view
+                    // {64 K, rows, K / 64}: the box lands as two 128B-swizzled tiles
+                    // of 64 (half <= 64, tiles 8 KB apart) or 128 rows (16 KB apart)
+                    tc::tma_load_3d(db, big ? &map_x2 : &map_x, fbar, 0, brow0, ku * 2);
                     issued_mask |= 1u << u;
                     issued_phase = (issued_phase & ~(1u << u)) | (pu << u);
                 }
@@ -297,7 +298,9 @@ tc_grouped_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const uint32_t a0 = tmem_base + A_COL0 + A_UNIT_COLS * a + BK / 2 * h;
-                            const uint32_t b0 = sB + u * 2 * B_BYTES + h * B_BYTES;
+                            // the second sub-stage follows the first: 64 rows (8 KB)
+                            // later for halves of at most 64 rows, else 128 (16 KB)
+                            const uint32_t b0 = sB + u * 2 * B_BYTES + h * (split ? B_BYTES / 2 : B_BYTES);
 #pragma unroll
                             for (int ks = 0; ks < BK / 16; ++ks) {
                                 tc::mma_f16_tmem_a_pair(d_tmem, a0 + 8 * ks, tc::sw128_kmajor_desc(b0 + ks * 32), idesc,
@@ -556,6 +559,20 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Activation rows [R][K] fp16 as a 3D view {64 K elements, rows, K / 64
+// chunks}: a box {64, box_rows, 2} is one unit's two sub-stages of box_rows
+// rows, each a 128B-swizzled K-major tile.
+bool make_x_map(CUtensorMap* m, const void* ptr, int K, int R, uint32_t box_rows) {
+    EncodeFn enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)BK, (cuuint64_t)R, (cuuint64_t)(K / BK)};
+    const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)BK * 2};
+    const cuuint32_t box[3] = {BK, box_rows, 2}, estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr size_t TC_SMEM_LIMIT = 232448;
 
 // Units of the shared-memory ring for a reduction length: 5 when they fit
@@ -601,10 +618,8 @@ cudaError_t launch_impl(int E, int d, int f, int R, const TcIn& in, cudaStream_t
                          CU_TENSOR_MAP_SWIZZLE_NONE)) {
         return cudaErrorInvalidValue;
     }
-    if (!make_map(&map_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, GATEUP ? in.x16 : in.h16, (uint64_t)p.K,
-                  (uint64_t)R, BK, B_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&map_x2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, GATEUP ? in.x16 : in.h16, (uint64_t)p.K,
-                  (uint64_t)R, BK, 2 * B_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_x_map(&map_x, GATEUP ? in.x16 : in.h16, p.K, R, B_BOX_ROWS) ||
+        !make_x_map(&map_x2, GATEUP ? in.x16 : in.h16, p.K, R, 2 * B_BOX_ROWS))
         return cudaErrorInvalidValue;
 
     const size_t smem = tc_smem_bytes(SU, p.K);
