@@ -174,9 +174,14 @@ class Workload:
         self.host_lg = [S.router_logits(cfg, l) for l in range(self.L)]
         log(f"[bench] generated {self.L} layer(s) of {cfg.name} in {time.time() - t0:.1f}s")
         self.layers = [M.Layer.from_numpy(w, device) for w in self.host_w]
-        self.x = [torch.from_numpy(x.view(np.int16)).to(device).view(torch.bfloat16) for x in self.host_x]
-        self.lg = [torch.from_numpy(g).to(device) for g in self.host_lg]
-        self.out = [torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=device) for _ in range(self.L)]
+        # every layer's activations, logits and outputs in one buffer each (the
+        # layers take views), so a step's inputs and outputs move in one copy each
+        self.x_all = torch.from_numpy(np.stack(self.host_x).view(np.int16)).to(device).view(torch.bfloat16)
+        self.lg_all = torch.from_numpy(np.stack(self.host_lg)).to(device)
+        self.out_all = torch.empty((self.L, cfg.T, cfg.d), dtype=torch.bfloat16, device=device)
+        self.x = [self.x_all[l] for l in range(self.L)]
+        self.lg = [self.lg_all[l] for l in range(self.L)]
+        self.out = [self.out_all[l] for l in range(self.L)]
         self.ids = [torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=device) for _ in range(self.L)]
         self.calls = [M.LayerCall(layer, cfg.T, cfg.k, device=device) for layer in self.layers]
         self.weight_bytes = sum(layer.nbytes() for layer in self.layers)
@@ -370,19 +375,19 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
     # ------------------------------------------------------------------ e2e
     e2e = None
     if want_e2e:
-        hx = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in wl.host_x]
-        hl = [torch.from_numpy(gl).pin_memory() for gl in wl.host_lg]
-        ho = [torch.empty((cfg.T, cfg.d), dtype=torch.int16).pin_memory() for _ in range(wl.L)]
-        h2d = sum(a.numel() * a.element_size() for a in hx) + sum(a.numel() * a.element_size() for a in hl)
-        d2h = sum(a.numel() * a.element_size() for a in ho)
+        # the step's inputs and outputs as one pinned buffer each: one copy in
+        # per tensor kind, one copy out
+        hx = torch.from_numpy(np.stack(wl.host_x).view(np.int16)).pin_memory()
+        hl = torch.from_numpy(np.stack(wl.host_lg)).pin_memory()
+        ho = torch.empty((wl.L, cfg.T, cfg.d), dtype=torch.int16).pin_memory()
+        h2d = hx.numel() * hx.element_size() + hl.numel() * hl.element_size()
+        d2h = ho.numel() * ho.element_size()
         with torch.cuda.stream(s):
             def e2e_step():
-                for l in range(wl.L):
-                    wl.x[l].view(torch.int16).copy_(hx[l], non_blocking=True)
-                    wl.lg[l].copy_(hl[l], non_blocking=True)
+                wl.x_all.view(torch.int16).copy_(hx, non_blocking=True)
+                wl.lg_all.copy_(hl, non_blocking=True)
                 g.replay()
-                for l in range(wl.L):
-                    ho[l].copy_(wl.out[l].view(torch.int16), non_blocking=True)
+                ho.copy_(wl.out_all.view(torch.int16), non_blocking=True)
             for _ in range(warmup):
                 e2e_step()
             s.synchronize()
