@@ -15,15 +15,15 @@
 //   B = activation rows of one expert segment (fp16, TMA, SW128 K-major)
 // The GEMM runs on CTA pairs (2-SM clusters, tcgen05 cta_group::2): each CTA
 // dequantises its own 128 weight rows into its own tensor memory and loads
-// half of the token tile, one thread of the even CTA issues the pair's MMAs,
-// and each CTA drains its 128 rows of the accumulator.  Per 64-K stage an SM
+// half of the token tile, one or two threads of the even CTA issue the pair's
+// MMAs, and each CTA drains its 128 rows of the accumulator.  Per 64 K an SM
 // then receives 16 KB of activations and 4 KB of codes (36 KB for one CTA
 // alone): the rate at which an SM's copies land, not the tensor pipe, bounded
-// the one-CTA stage.
+// the one-CTA kernel.
 // The pipeline moves in units of 128 K (two 64-K sub-stages, one scale
-// group): one barrier round, one copy of codes and one wait per unit.  The
-// shared-memory ring holds one unit more than tensor memory holds A units, so
-// the copies are issued one unit earlier.
+// group): one barrier round, one copy of codes, one copy of activations and
+// one wait per unit.  The shared-memory ring holds one unit more than tensor
+// memory holds A units, so the copies are issued one unit earlier.
 // The operands are fp16 rather than bf16: bf16 activations convert to fp16
 // exactly inside fp16's range (values outside set the error word), and a
 // weight is q s - fl16(z s) rounded once to fp16, which keeps 3 more bits than
@@ -41,11 +41,11 @@
 // layer's own combine, bf16 when y is the caller's output).
 //
 // Warp roles (896 threads per CTA): 0 TMA producer, 1 TMEM owner and (even
-// CTA) MMA issuer, 2-3 idle, 4-11 dequantisation (warp w: TMEM lane quarter
-// w % 4, half (w - 4) / 4 of a sub-stage's K), 12-27 epilogue (warp w: lane
-// quarter w % 4, every fourth 32-column block).  With one accumulator the
-// next item's MMAs wait until both CTAs' epilogues have read it, so four
-// warps per quarter cut that wait.
+// CTA) MMA issuer 0, 2 (even CTA) MMA issuer 1, 3 idle, 4-11 dequantisation
+// (warp w: TMEM lane quarter w % 4, half (w - 4) / 4 of each sub-stage's K),
+// 12-27 epilogue (warp w: lane quarter w % 4, every fourth 32-column block).
+// With one accumulator the next item's MMAs wait until both CTAs' epilogues
+// have read it, so four warps per quarter cut that wait.
 // Barriers: each CTA's copies land on its own full[u]; both CTAs' dequant
 // warps arrive on the even CTA's afull[a] and both epilogues on its
 // accempty; MMA completion (empty[u], aempty[a], accfull, done) is signalled
