@@ -276,6 +276,16 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
     // here on global memory (inputs, workspace, outputs) is read and written,
     // so wait until the previous grid has completed and its writes are
     // visible.  (Without a programmatic dependency this returns at once.)
+    // Before that, one warp asks L2 for this layer's logits and activations,
+    // the first data the layer reads: a prefetch returns nothing, so it is
+    // harmless even while the previous kernel may still write them.
+    if (warp == 2) {
+        const int lg_lines = (T * E * 4 + 127) / 128, x_lines = (T * d * 2 + 127) / 128;
+        for (int i = lane; i < lg_lines; i += 32)
+            asm volatile("prefetch.global.L2 [%0];" :: "l"(reinterpret_cast<const char*>(p.logits) + 128 * (size_t)i));
+        for (int i = lane; i < x_lines; i += 32)
+            asm volatile("prefetch.global.L2 [%0];" :: "l"(reinterpret_cast<const char*>(p.x) + 128 * (size_t)i));
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (warp < nsort) {
         if (warp < T) {
