@@ -41,8 +41,9 @@ struct AlignOut {
 };
 constexpr int ALIGN_SMALL_MAX_R = 2048;   // single-CTA permutation up to this many rows
 constexpr int ALIGN_BLOCK_ROWS = 1024;    // most assignments per CTA on the multi-block path
-// Assignments per CTA on the multi-block path: 256 (more CTAs for the stable
-// scatter) while the per-block count table stays within 64 KB, else 1024.
+// Assignments per CTA on the multi-block path: the smallest of 32, 64 and 256
+// (more CTAs for the stable placement and the row copy) whose per-block count
+// table stays within 64 KB, else 1024.
 int align_block_rows(int R, int E);
 size_t align_blockcnt_bytes(int R, int E);
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, const uint16_t* x, int d,

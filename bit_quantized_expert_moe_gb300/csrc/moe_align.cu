@@ -373,7 +373,12 @@ __global__ void __launch_bounds__(SCAN_THREADS) plan_from_offsets_kernel(const i
 }  // namespace
 
 int align_block_rows(int R, int E) {
-    return (size_t)ceil_div(R, 256) * E * sizeof(int32_t) <= 65536 ? 256 : ALIGN_BLOCK_ROWS;
+    // the smallest of 32, 64, 256 whose per-block count table fits in 64 KB:
+    // more placing CTAs (each copies its own rows once they are enough to
+    // fill the GPU); else 1024
+    for (const int rows : {32, 64, 256})
+        if ((size_t)ceil_div(R, rows) * E * sizeof(int32_t) <= 65536) return rows;
+    return ALIGN_BLOCK_ROWS;
 }
 
 size_t align_blockcnt_bytes(int R, int E) {
