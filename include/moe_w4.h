@@ -220,9 +220,10 @@ moe_status_t moe_combine(const void* y_perm_bf16, const int32_t* inv, const floa
  * every CTA, gate_up, one grid barrier, down with the combine fused; one CTA
  * per SM, cooperative launch).  Consecutive calls on a stream may be launched
  * as programmatic dependents of the previous kernel: a call's CTAs start their
- * shared-memory setup early but touch no global memory (inputs, outputs,
- * workspace) before the previous kernel on the stream has completed, so stream
- * order is unchanged.  Its intermediate precision: activations and h
+ * shared-memory setup early but read and write no global memory (inputs,
+ * outputs, workspace) before the previous kernel on the stream has completed,
+ * so stream order is unchanged; early on they only hint L2 to fetch x and
+ * logits, a prefetch that returns no value.  Its intermediate precision: activations and h
  * in fp16 (|x|, |h| < 65504, else MOE_ERR_F16_RANGE), products of the exact
  * int4 codes with fp32 accumulation, zero and scale applied per group of 128
  * in fp32.  MOE_W4_DECODE_KERNEL=split runs the stage chain instead.
