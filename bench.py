@@ -186,9 +186,16 @@ class Workload:
         self.calls = [M.LayerCall(layer, cfg.T, cfg.k, device=device) for layer in self.layers]
         self.weight_bytes = sum(layer.nbytes() for layer in self.layers)
 
-    def step(self, stream):
+    def step(self, stream, bufs=None):
+        x, lg, out = (self.x_all, self.lg_all, self.out_all) if bufs is None else bufs
         for l in range(self.L):
-            self.calls[l](self.x[l], self.lg[l], self.out[l], self.ids[l], stream=stream)
+            self.calls[l](x[l], lg[l], out[l], self.ids[l], stream=stream)
+
+    def second_buffers(self, torch):
+        """Another set of input and output buffers with the same contents, so a
+        step can compute on one set while the next step's inputs arrive in the
+        other."""
+        return self.x_all.clone(), self.lg_all.clone(), torch.empty_like(self.out_all)
 
     def tokens_per_step(self):
         return self.cfg.T * self.L
@@ -382,27 +389,86 @@ def measure(M, torch, wl, steps, warmup, rank, world, peaks, peak_src, want_e2e=
         ho = torch.empty((wl.L, cfg.T, cfg.d), dtype=torch.int16).pin_memory()
         h2d = hx.numel() * hx.element_size() + hl.numel() * hl.element_size()
         d2h = ho.numel() * ho.element_size()
+        # serial: copy in, compute, copy out, one step after the other on one stream
         with torch.cuda.stream(s):
-            def e2e_step():
+            def serial_step():
                 wl.x_all.view(torch.int16).copy_(hx, non_blocking=True)
                 wl.lg_all.copy_(hl, non_blocking=True)
                 g.replay()
                 ho.copy_(wl.out_all.view(torch.int16), non_blocking=True)
             for _ in range(warmup):
-                e2e_step()
+                serial_step()
             s.synchronize()
             if world > 1:
                 torch.distributed.barrier()
             a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a0.record(s)
             for _ in range(steps):
-                e2e_step()
+                serial_step()
             a1.record(s)
             s.synchronize()
+        _, serial_ms = job_rate(torch, a0.elapsed_time(a1) / steps, wl.tokens_per_step(), world, dev)
+
+        # double-buffered, as a serving loop runs it: two input/output buffer
+        # sets, one graph per set; step i's inputs are copied in on a copy
+        # stream while step i-1 computes, and its outputs copied out on another
+        # while step i+1 computes.  Every step still copies all of its inputs
+        # in and all of its outputs out inside the timed region.
+        bufs = [(wl.x_all, wl.lg_all, wl.out_all), wl.second_buffers(torch)]
+        hos = [ho, torch.empty_like(ho).pin_memory()]
+        graphs = [g, torch.cuda.CUDAGraph()]
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graphs[1], stream=s):
+                wl.step(s, bufs[1])
+        s.synchronize()
+        cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+        in_ready, computed, out_read = ([torch.cuda.Event(), torch.cuda.Event()] for _ in range(3))
+        used = [False, False]
+
+        def pipelined_steps(n, start):
+            start.record(s)
+            cin.wait_event(start)
+            for i in range(n):
+                b = i & 1
+                xb, lb, ob = bufs[b]
+                with torch.cuda.stream(cin):
+                    if used[b]:
+                        cin.wait_event(computed[b])   # step i-2 has read this set's inputs
+                    xb.view(torch.int16).copy_(hx, non_blocking=True)
+                    lb.copy_(hl, non_blocking=True)
+                    in_ready[b].record(cin)
+                with torch.cuda.stream(s):
+                    s.wait_event(in_ready[b])
+                    if used[b]:
+                        s.wait_event(out_read[b])     # step i-2's outputs have left
+                    graphs[b].replay()
+                    computed[b].record(s)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(computed[b])
+                    hos[b].copy_(ob.view(torch.int16), non_blocking=True)
+                    out_read[b].record(cout)
+                used[b] = True
+            for b in range(2):
+                if used[b]:
+                    s.wait_event(out_read[b])
+
+        pipelined_steps(warmup, torch.cuda.Event())
+        s.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        pipelined_steps(steps, a0)
+        a1.record(s)
+        s.synchronize()
+        for hb in hos[1:]:
+            if not torch.equal(hb, hos[0]):
+                raise RuntimeError("the two buffer sets' outputs differ")
         e2e_value, ems = job_rate(torch, a0.elapsed_time(a1) / steps, wl.tokens_per_step(), world, dev)
         e2e = {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ems, 4),
-               "path": "pinned host x/logits -> device, graph replay of moe_layer_forward x L, out -> pinned host"}
+               "serial_ms_per_step": round(serial_ms, 4),
+               "path": "pinned host x/logits -> device, graph replay of moe_layer_forward x L, out -> pinned "
+                       "host; double-buffered (copies of neighbouring steps overlap this step's compute)"}
 
     return {
         "value": value, "ms_per_step": ms, "eager_ms_per_step": eager_ms, "roofline": roofline,
