@@ -930,10 +930,15 @@ cudaError_t launch_decode_fused(const FusedIn& in, cudaStream_t s) {
     // fp16 scales and zeros [rows][groups]: by TMA when a row is a multiple of
     // 16 bytes (groups % 8 == 0): gate_up {groups, feature, expert * 2 + half}
     // box {8, 8, 2}, down {groups, row} box {8, 16}; by bulk copies when a row
-    // fits one chunk (groups < 8; 16-byte aligned arrays); else with cp.async
+    // fits one chunk (groups < 8; 16-byte aligned arrays); else with cp.async.
+    // In the 3-pipeline instantiation (little weight per CTA) gate_up's scales
+    // and zeros always go by the producer lanes' 4-byte cp.async: measured on
+    // the d_model 2048 layer 17.45 against 17.95 us per layer with the TMA
+    // boxes (outputs identical); on the d_model 7168 layer (4 pipelines) the
+    // TMA boxes are the faster, 75.4 against 79.4 us.
     CUtensorMap m13s = m13, m13z = m13, m2s = m2, m2z = m2;
     const uint64_t Gd = (uint64_t)d / 128, Gf = (uint64_t)f / 128;
-    bool sz13 = Gd % 8 == 0, sz2 = Gf % 8 == 0;
+    bool sz13 = Gd % 8 == 0 && nq == 4, sz2 = Gf % 8 == 0;
     auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
     if (sz13) {
         const uint64_t dims[3] = {Gd, (uint64_t)f, (uint64_t)E * 2}, str[2] = {Gd * 2, (uint64_t)f * Gd * 2};
