@@ -45,8 +45,8 @@
 // CW + i owns 1/NQ of the ring's slots and feeds consumer pairs 2i and 2i + 1,
 // in chunk order.  A chunk is 16 weight rows x 4 lines of 128 B (2 groups
 // each; one TMA box, 128-byte swizzle) plus the rows' fp16 scales and zeros
-// (TMA boxes, plain bulk copies or 4-byte cp.async, by shape), all completing
-// the chunk's full mbarrier.  Consumer warps 0 .. CW - 1 form pairs; each warp
+// (TMA boxes, plain bulk copies or 4-byte cp.async, by shape and
+// instantiation), all completing the chunk's full mbarrier.  Consumer warps 0 .. CW - 1 form pairs; each warp
 // of a pair takes half of a chunk's groups, loading each group's codes into
 // registers right before its math and releasing the slot after the last
 // group's loads; the two halves are added through shared memory.
@@ -398,11 +398,10 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap map13, const __grid_cons
 
     // ---------------------------------------------------------- producers
     // Per chunk the pipeline waits until the chunk's slot is empty and issues
-    // the TMA box of the codes.  The fp16 scales and zeros come by TMA as well
-    // where a row's groups are a multiple of 8 (16-byte rows: then one lane
-    // does all of it), else every lane copies its row's values with 4-byte
-    // cp.async and a counted arrival before lane 0 arrives with the byte
-    // count.  One warp per pipeline, in chunk order: a slot's round r is
+    // the TMA box of the codes.  The fp16 scales and zeros come by TMA or bulk
+    // copies issued by lane 0 as well, or every lane copies its row's values
+    // with 4-byte cp.async and a counted arrival before lane 0 arrives with
+    // the byte count (the host picks the form per phase: sz13_mode, sz2_mode).  One warp per pipeline, in chunk order: a slot's round r is
     // waited on only after its round r - 1 has completed, so every parity
     // wait is exact.
     if (warp >= PRODUCER_WARP) {
